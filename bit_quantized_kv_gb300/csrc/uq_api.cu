@@ -1,0 +1,223 @@
+// uq_api.cu -- host side of the C ABI declared in include/uq.h: argument
+// validation, error reporting, the device error word, and kernel launches.
+// Nothing here allocates device memory or synchronises, except
+// uq_check_device_error, which is documented to.
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "uq.h"
+#include "uq_device.cuh"
+
+namespace uq {
+cudaError_t launch_store(bool rotated_f32, const void* key, const void* value, void* kv_cache,
+                         const int64_t* slot_mapping, int64_t num_tokens, int Hk,
+                         int64_t key_stride, int64_t value_stride, int block_size,
+                         int64_t num_slots, unsigned* err, cudaStream_t stream);
+cudaError_t launch_decode(const uint16_t* query, int64_t q_ss, int64_t q_sh, const uint8_t* kv,
+                          const int32_t* bt, const int32_t* sl, float scale, int B, int Hq,
+                          int Hk, int num_blocks, int max_blocks, int S, void* workspace,
+                          uint16_t* out, unsigned* err, cudaStream_t stream,
+                          cudaEvent_t ev_before_stage1, cudaEvent_t ev_after_stage1);
+}  // namespace uq
+
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+constexpr int kMaxDevices = 64;
+
+thread_local char g_last_error[512] = "";
+thread_local cudaEvent_t g_ev_before_stage1 = nullptr;
+thread_local cudaEvent_t g_ev_after_stage1 = nullptr;
+
+// The device error word.  Kernels receive its device address; host code
+// obtains that address once per device with cudaGetSymbolAddress.
+__device__ unsigned int g_device_error_word;
+unsigned int* g_err_ptr[kMaxDevices] = {nullptr};
+std::mutex g_err_mutex;
+
+uq_status fail(uq_status code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+uq_status ok() {
+  g_last_error[0] = '\0';
+  return UQ_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Device address of the error word on the current device (set-up on first use).
+uq_status error_word(unsigned int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(UQ_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(UQ_ERR_UNSUPPORTED, "device index %d >= %d", dev, kMaxDevices);
+  std::lock_guard<std::mutex> lock(g_err_mutex);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_device_error_word);
+    if (e != cudaSuccess) return fail(UQ_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    g_err_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  *out = g_err_ptr[dev];
+  return UQ_OK;
+}
+
+uq_status check_store_args(const void* key, const void* value, void* kv_cache,
+                           const int64_t* slot_mapping, int64_t num_tokens, int Hk, int D,
+                           int num_blocks, int block_size, int slot_bytes, size_t elem_bytes) {
+  if (num_tokens < 0) return fail(UQ_ERR_INVALID_ARG, "num_tokens %lld < 0", (long long)num_tokens);
+  if (D != uq::kHeadDim) return fail(UQ_ERR_UNSUPPORTED, "head_dim %d unsupported (only 256)", D);
+  if (slot_bytes != uq::kSlotBytes) return fail(UQ_ERR_INVALID_ARG, "slot_bytes %d != 272", slot_bytes);
+  if (Hk < 1) return fail(UQ_ERR_INVALID_ARG, "num_kv_heads %d < 1", Hk);
+  if (num_blocks < 1 || block_size < 1)
+    return fail(UQ_ERR_INVALID_ARG, "num_blocks %d / block_size %d must be >= 1", num_blocks, block_size);
+  if (num_tokens == 0) return UQ_OK;
+  if (!key || !value || !kv_cache || !slot_mapping)
+    return fail(UQ_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(key, 16) || !aligned(value, 16) || !aligned(kv_cache, 16))
+    return fail(UQ_ERR_INVALID_ARG, "key, value and kv_cache must be 16-byte aligned");
+  if (!aligned(slot_mapping, 8)) return fail(UQ_ERR_INVALID_ARG, "slot_mapping must be 8-byte aligned");
+  if (num_tokens > (int64_t)1 << 40 || (int64_t)Hk * num_tokens > ((int64_t)1 << 36))
+    return fail(UQ_ERR_INVALID_ARG, "num_tokens * num_kv_heads too large");
+  (void)elem_bytes;
+  return UQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int uq_version(void) { return kVersion; }
+
+size_t uq_slot_bytes(int head_dim) {
+  return head_dim == uq::kHeadDim ? (size_t)uq::kSlotBytes : 0;
+}
+
+size_t uq_decode_workspace_bytes(int B, int Hq, int head_dim, int max_num_kv_splits) {
+  if (B < 0 || Hq < 1 || head_dim != uq::kHeadDim || max_num_kv_splits < 1 || max_num_kv_splits > 256)
+    return 0;
+  const size_t rows = (size_t)B * Hq * max_num_kv_splits;
+  const size_t bytes = rows * (head_dim + 1) * sizeof(float);
+  return (bytes + 255) / 256 * 256;
+}
+
+const char* uq_last_error(void) { return g_last_error; }
+
+uq_status uq_set_timing_events(void* before_stage1, void* after_stage1) {
+  g_ev_before_stage1 = static_cast<cudaEvent_t>(before_stage1);
+  g_ev_after_stage1 = static_cast<cudaEvent_t>(after_stage1);
+  return UQ_OK;
+}
+
+uq_status uq_store(const void* key, const void* value, void* kv_cache, const int64_t* slot_mapping,
+                   int64_t num_tokens, int num_kv_heads, int head_dim, int num_blocks,
+                   int block_size, int slot_bytes, int64_t key_stride_tok,
+                   int64_t value_stride_tok, void* stream) {
+  uq_status st = check_store_args(key, value, kv_cache, slot_mapping, num_tokens, num_kv_heads,
+                                  head_dim, num_blocks, block_size, slot_bytes, 2);
+  if (st != UQ_OK) return st;
+  if (num_tokens == 0) return ok();
+  const int64_t row = (int64_t)num_kv_heads * head_dim;
+  if (key_stride_tok < row || value_stride_tok < row || key_stride_tok % 8 || value_stride_tok % 8)
+    return fail(UQ_ERR_INVALID_ARG, "token strides (%lld, %lld) must be >= Hk*D and multiples of 8",
+                (long long)key_stride_tok, (long long)value_stride_tok);
+  unsigned int* err = nullptr;
+  if ((st = error_word(&err)) != UQ_OK) return st;
+  cudaError_t e = uq::launch_store(false, key, value, kv_cache, slot_mapping, num_tokens,
+                                   num_kv_heads, key_stride_tok, value_stride_tok, block_size,
+                                   (int64_t)num_blocks * block_size, err,
+                                   static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(UQ_ERR_CUDA, "store launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+uq_status uq_store_rotated_f32(const float* key_rot, const float* value, void* kv_cache,
+                               const int64_t* slot_mapping, int64_t num_tokens, int num_kv_heads,
+                               int head_dim, int num_blocks, int block_size, int slot_bytes,
+                               void* stream) {
+  uq_status st = check_store_args(key_rot, value, kv_cache, slot_mapping, num_tokens, num_kv_heads,
+                                  head_dim, num_blocks, block_size, slot_bytes, 4);
+  if (st != UQ_OK) return st;
+  if (num_tokens == 0) return ok();
+  unsigned int* err = nullptr;
+  if ((st = error_word(&err)) != UQ_OK) return st;
+  cudaError_t e = uq::launch_store(true, key_rot, value, kv_cache, slot_mapping, num_tokens,
+                                   num_kv_heads, 0, 0, block_size, (int64_t)num_blocks * block_size,
+                                   err, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(UQ_ERR_CUDA, "store launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+uq_status uq_decode(const void* query, const void* kv_cache, const int32_t* block_table,
+                    const int32_t* seq_lens, float scale, int max_num_kv_splits, void* workspace,
+                    size_t workspace_bytes, void* out, int B, int Hq, int Hk, int head_dim,
+                    int num_blocks, int block_size, int max_blocks_per_seq, int slot_bytes,
+                    int64_t q_stride_seq, int64_t q_stride_head, void* stream) {
+  if (B < 0) return fail(UQ_ERR_INVALID_ARG, "B %d < 0", B);
+  if (head_dim != uq::kHeadDim) return fail(UQ_ERR_UNSUPPORTED, "head_dim %d unsupported (only 256)", head_dim);
+  if (slot_bytes != uq::kSlotBytes) return fail(UQ_ERR_INVALID_ARG, "slot_bytes %d != 272", slot_bytes);
+  if (block_size != 16) return fail(UQ_ERR_UNSUPPORTED, "block_size %d unsupported (only 16)", block_size);
+  if (Hk < 1 || Hq < 1 || Hq % Hk) return fail(UQ_ERR_INVALID_ARG, "Hq %d must be a positive multiple of Hk %d", Hq, Hk);
+  const int QG = Hq / Hk;
+  if (QG != 6 && QG != 8 && QG != 16) return fail(UQ_ERR_UNSUPPORTED, "query heads per kv head %d unsupported (6, 8, 16)", QG);
+  if (max_num_kv_splits < 1 || max_num_kv_splits > 256)
+    return fail(UQ_ERR_INVALID_ARG, "max_num_kv_splits %d outside [1, 256]", max_num_kv_splits);
+  if (num_blocks < 1 || max_blocks_per_seq < 1)
+    return fail(UQ_ERR_INVALID_ARG, "num_blocks %d / max_blocks_per_seq %d must be >= 1", num_blocks, max_blocks_per_seq);
+  if (B > 65535 || Hk > 65535) return fail(UQ_ERR_INVALID_ARG, "B %d or Hk %d exceeds the grid limit 65535", B, Hk);
+  if (!(scale == scale)) return fail(UQ_ERR_INVALID_ARG, "scale is NaN");
+  if (B == 0) return ok();
+  if (!query || !kv_cache || !block_table || !seq_lens || !workspace || !out)
+    return fail(UQ_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(query, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(workspace, 16))
+    return fail(UQ_ERR_INVALID_ARG, "query, kv_cache, workspace and out must be 16-byte aligned");
+  if (!aligned(block_table, 4) || !aligned(seq_lens, 4))
+    return fail(UQ_ERR_INVALID_ARG, "block_table and seq_lens must be 4-byte aligned");
+  if (q_stride_head < head_dim || q_stride_seq < (int64_t)(Hq - 1) * q_stride_head + head_dim ||
+      q_stride_head % 8 || q_stride_seq % 8)
+    return fail(UQ_ERR_INVALID_ARG, "query strides (%lld, %lld) must cover a [Hq][256] row and be multiples of 8",
+                (long long)q_stride_seq, (long long)q_stride_head);
+  const size_t need = uq_decode_workspace_bytes(B, Hq, head_dim, max_num_kv_splits);
+  if (workspace_bytes < need)
+    return fail(UQ_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu required", workspace_bytes, need);
+  unsigned int* err = nullptr;
+  uq_status st = error_word(&err);
+  if (st != UQ_OK) return st;
+  cudaError_t e = uq::launch_decode(static_cast<const uint16_t*>(query), q_stride_seq, q_stride_head,
+                                    static_cast<const uint8_t*>(kv_cache), block_table, seq_lens, scale,
+                                    B, Hq, Hk, num_blocks, max_blocks_per_seq, max_num_kv_splits,
+                                    workspace, static_cast<uint16_t*>(out), err,
+                                    static_cast<cudaStream_t>(stream), g_ev_before_stage1,
+                                    g_ev_after_stage1);
+  if (e != cudaSuccess) return fail(UQ_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+uq_status uq_check_device_error(void* stream, unsigned int* flags_out) {
+  unsigned int* err = nullptr;
+  uq_status st = error_word(&err);
+  if (st != UQ_OK) return st;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(UQ_ERR_CUDA, "cudaStreamSynchronize: %s", cudaGetErrorString(e));
+  unsigned int flags = 0;
+  e = cudaMemcpyFromSymbol(&flags, g_device_error_word, sizeof flags);
+  if (e != cudaSuccess) return fail(UQ_ERR_CUDA, "reading the error word: %s", cudaGetErrorString(e));
+  const unsigned int zero = 0;
+  e = cudaMemcpyToSymbol(g_device_error_word, &zero, sizeof zero);
+  if (e != cudaSuccess) return fail(UQ_ERR_CUDA, "clearing the error word: %s", cudaGetErrorString(e));
+  if (flags_out) *flags_out = flags;
+  if (flags) return fail(UQ_ERR_DEVICE_FLAG, "device error word 0x%x", flags);
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,203 @@
+// uq_device.cuh -- device-side helpers shared by the store and decode kernels:
+// documented PTX conversions (E2M1, E4M3, f16), warp MMA, bulk async copies
+// and bounded mbarrier waits.  sm_103a only.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace uq {
+
+constexpr int kHeadDim = 256;
+constexpr int kSlotBytes = 272;          // 128 K codes + 128 V codes + 8 + 8 scales
+constexpr int kKScaleOff = 256;
+constexpr int kVScaleOff = 264;
+constexpr int kVCodeOff = 128;
+
+// Iteration cap of every spin-wait (about a second of polling): a wait that
+// runs out sets UQ_DEVERR_TIMEOUT and the kernel returns instead of hanging.
+constexpr uint32_t kWaitSpinLimit = 1u << 24;
+
+constexpr unsigned kErrBadPage = 1u;
+constexpr unsigned kErrBadSlot = 2u;
+constexpr unsigned kErrTimeout = 4u;
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) {
+  return __uint_as_float(bits16 << 16);
+}
+
+// Two fp32 -> one byte of two E2M1 codes: `lo` in bits 0-3, `hi` in bits 4-7.
+// Round to nearest even, saturating at +-6 (cvt ... satfinite).  The sign bit
+// of each nibble is then forced to the sign of its input, so a negative value
+// that rounds to zero is stored with its sign.
+__device__ __forceinline__ uint32_t e2m1x2_from_f32(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n}\n"
+      : "=r"(r) : "f"(hi), "f"(lo));
+  r |= ((__float_as_uint(lo) >> 28) & 0x8u) | ((__float_as_uint(hi) >> 24) & 0x80u);
+  return r;
+}
+
+// One byte of two E2M1 codes -> f16x2 (low nibble in the low half).  Exact.
+__device__ __forceinline__ uint32_t f16x2_from_e2m1x2(uint32_t byte_in_low_bits) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n}\n"
+      : "=r"(r) : "r"(byte_in_low_bits));
+  return r;
+}
+
+// Four bytes of a word, each two E2M1 codes -> four f16x2 registers.
+__device__ __forceinline__ void f16x2x4_from_e2m1_word(uint32_t w, uint32_t (&o)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n}\n"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3]) : "r"(w));
+}
+
+// Two fp32 -> E4M3 (round to nearest even, saturating at +-448) -> f16x2
+// holding those E4M3 values exactly; `lo` lands in the low half.
+__device__ __forceinline__ uint32_t e4m3_roundtrip_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %1, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, t;\n}\n"
+      : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+  return r;
+}
+
+// D = A * B + D, m16n8k16, f16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3, uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, "
+      "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+__device__ __forceinline__ float fast_log2(float x) {
+  float r;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// 2^(byte - 127) as fp32, exact for every byte in [0, 254] (byte 0 is the
+// subnormal 2^-127).
+__device__ __forceinline__ float ue8m0_to_f32(uint32_t byte) {
+  return byte ? __uint_as_float(byte << 23) : __uint_as_float(1u << 22);
+}
+
+// 2^-delta as f16 bits (delta >= 0): exact down to 2^-24, 0 below.
+__device__ __forceinline__ uint32_t pow2_neg_f16(int delta) {
+  delta = delta > 126 ? 126 : delta;
+  float f = __uint_as_float((uint32_t)(127 - delta) << 23);
+  unsigned short h;
+  asm("cvt.rn.f16.f32 %0, %1;" : "=h"(h) : "f"(f));
+  return h;
+}
+
+// Largest of the eight bytes of (lo, hi).
+__device__ __forceinline__ uint32_t max_byte8(uint32_t lo, uint32_t hi) {
+  uint32_t m = __vmaxu4(lo, hi);
+  m = __vmaxu4(m, m >> 16);
+  m = __vmaxu4(m, m >> 8);
+  return m & 0xffu;
+}
+
+// ---------------------------------------------------------------------------
+// Shared-memory addresses, mbarriers and bulk async copies (TMA engine).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
+               :: "r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+
+// Bounded wait for the phase with the given parity to complete.  Returns
+// false if the iteration cap ran out.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (uint32_t it = 0; it < kWaitSpinLimit; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Global -> shared bulk copy of `bytes` (multiple of 16, both addresses
+// 16-byte aligned), completing on mbarrier `bar` with a tx-count of `bytes`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint4 ldg_nc_128(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+}  // namespace uq

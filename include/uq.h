@@ -1,0 +1,195 @@
+/*
+ * uq.h -- C ABI of the UltraQuant 4-bit KV-cache library for NVIDIA GB300
+ * (sm_103a): paged store into an FP4 E2M1 + UE8M0 cache with a Hadamard-
+ * rotated K, and split-KV paged decode attention over that cache.
+ *
+ * Sources (vLLM API documentation pages):
+ *   vllm.v1.attention.backends.ultraquant_attn, UltraQuantAttentionImpl
+ *     (class docstring: "FP4 E2M1 + UE8M0, rotated K"; _ensure_on_device:
+ *     the Hadamard rotation; _store_kv: the store seam; _decode_attention:
+ *     the decode seam and its workspace)
+ *   vllm.v1.attention.ops.flydsl_ultraquant_decode
+ *     (flydsl_ultraquant_decode_attention: query prologue with the E4M3
+ *     haircut, stage-1 launch, partition reduce; _fp4_value_lut)
+ *   vllm.v1.attention.ops.turboquant_soa.triton_turboquant_decode_v2
+ *     (triton_turboquant_decode_attention_v2: fixed split count for graph
+ *     capture, split partials and their combine)
+ *
+ * Conventions shared by every entry point
+ *   - All tensor arguments are DEVICE pointers owned by the caller.  The
+ *     library allocates no memory and never synchronises inside uq_store,
+ *     uq_store_rotated_f32 or uq_decode; work is enqueued on `stream`
+ *     (a cudaStream_t passed as void*; NULL is the legacy default stream).
+ *   - Arguments are validated on the host before anything is enqueued; an
+ *     invalid call returns an error code and enqueues nothing.  The message
+ *     of the last error on the calling thread is in uq_last_error().
+ *   - Index errors that only the device can see (a page id outside
+ *     [0, num_blocks), a slot beyond the cache) never fault: the affected
+ *     token is skipped and a bit is set in a device error word that
+ *     uq_check_device_error() reads.
+ *   - Supported shapes: head_dim D = 256, block_size 16, query heads per KV
+ *     head (Hq / Hk) in {6, 8, 16}; other values return UQ_ERR_UNSUPPORTED.
+ *
+ * Cache layout (the pages give only kv_cache's shape, (num_blocks,
+ * block_size, Hk, slot_size) uint8; the byte layout below is this library's)
+ *   Slot of (page p, offset o, kv head h) starts at byte
+ *   ((p * block_size + o) * Hk + h) * slot_bytes, slot_bytes = 272 for D = 256:
+ *     [  0,128) K codes: element 2j in the low nibble of byte j, 2j+1 high
+ *     [128,256) V codes, same packing
+ *     [256,264) K block-scale bytes, one UE8M0 per 32 consecutive elements
+ *     [264,272) V block-scale bytes
+ *   A code c decodes to E2M1(c) * 2^(byte - 127), E2M1 codes 0..7 being
+ *   +{0, .5, 1, 1.5, 2, 3, 4, 6} and 8..15 their negatives.  K is stored
+ *   rotated: k_rot = k H with H[i][j] = (-1)^popcount(i&j) / 16.  V is not
+ *   rotated.
+ */
+#ifndef UQ_H
+#define UQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    UQ_OK = 0,
+    UQ_ERR_INVALID_ARG = 1,          /* null/misaligned pointer, bad size or stride */
+    UQ_ERR_UNSUPPORTED = 2,          /* a shape outside the supported set */
+    UQ_ERR_WORKSPACE_TOO_SMALL = 3,  /* workspace_bytes < uq_decode_workspace_bytes() */
+    UQ_ERR_CUDA = 4,                 /* a CUDA runtime call or launch failed */
+    UQ_ERR_DEVICE_FLAG = 5           /* the device error word was non-zero */
+} uq_status;
+
+/* Device error word bits (uq_check_device_error). */
+#define UQ_DEVERR_BAD_PAGE 1u        /* block_table entry outside [0, num_blocks) */
+#define UQ_DEVERR_BAD_SLOT 2u        /* slot_mapping entry >= num_blocks * block_size */
+#define UQ_DEVERR_TIMEOUT  4u        /* a bounded wait on an async copy gave up */
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int uq_version(void);
+
+/* Bytes of one (token, kv head) slot for head_dim: D + D/16 (272 for D = 256).
+ * Returns 0 for an unsupported head_dim. */
+size_t uq_slot_bytes(int head_dim);
+
+/*
+ * Workspace bytes uq_decode needs for a batch of up to B sequences with Hq
+ * query heads and max_num_kv_splits splits: the per-split partial outputs
+ * (fp32, D values) and their log-sum-exp (fp32) for every (sequence, query
+ * head, split), i.e. B * Hq * S * (D + 1) * 4, rounded up to 256 bytes.  It
+ * depends only on its arguments, so a caller can size the workspace once for
+ * its largest batch before capturing a CUDA graph (the reference pre-grows
+ * its pool before capture for the same reason, _ensure_on_device and
+ * _SegmBufPool).  Returns 0 for invalid arguments.
+ */
+size_t uq_decode_workspace_bytes(int B, int Hq, int head_dim, int max_num_kv_splits);
+
+/*
+ * uq_store -- rotate K by the Hadamard matrix and pack K and V into the
+ * paged FP4 cache (ultraquant_attn, UltraQuantAttentionImpl._store_kv).
+ *
+ *   key, value    bf16, element (n, h, d) at n * key_stride_tok + h * D + d
+ *                 (value_stride_tok for value); 16-byte aligned, strides in
+ *                 elements and multiples of 8.
+ *   kv_cache      uint8 [num_blocks][block_size][Hk][slot_bytes], written.
+ *   slot_mapping  int64 [num_tokens]; token n goes to slot slot_mapping[n]
+ *                 (page = slot / block_size, offset = slot % block_size).
+ *                 A negative slot skips the token; a slot >= num_blocks *
+ *                 block_size skips it and sets UQ_DEVERR_BAD_SLOT.
+ *
+ * Per (token, head): K is converted to fp32 (exact), transformed by the
+ * unnormalised fast Walsh-Hadamard butterfly in the fixed stage order
+ * h = 1, 2, ..., 128 (pair (i, i+h) -> (a+b, a-b)) and multiplied by 1/16.
+ * Each 32-element block of rotated K and of V gets the UE8M0 byte
+ * max(0, biased_exponent(amax) - 2) (shared exponent floor(log2 amax) - 2,
+ * clamped at -127) and E2M1 codes of x * 2^-(byte-127), rounded to nearest
+ * even with saturation at +-6; a negative value that rounds to zero keeps
+ * its sign bit.  num_tokens == 0 is a no-op.
+ */
+uq_status uq_store(const void *key, const void *value, void *kv_cache,
+                   const int64_t *slot_mapping, int64_t num_tokens,
+                   int num_kv_heads, int head_dim, int num_blocks, int block_size,
+                   int slot_bytes, int64_t key_stride_tok, int64_t value_stride_tok,
+                   void *stream);
+
+/*
+ * uq_store_rotated_f32 -- the quantise-and-pack half of uq_store for K that
+ * is already rotated: key_rot and value are fp32, contiguous
+ * [num_tokens][Hk][D], 16-byte aligned.  Same slot rules, scale rule and
+ * rounding as uq_store, without the rotation.  It lets a caller check the
+ * packed bytes against another implementation that quantises the same fp32
+ * rotated K.
+ */
+uq_status uq_store_rotated_f32(const float *key_rot, const float *value,
+                               void *kv_cache, const int64_t *slot_mapping,
+                               int64_t num_tokens, int num_kv_heads, int head_dim,
+                               int num_blocks, int block_size, int slot_bytes,
+                               void *stream);
+
+/*
+ * uq_decode -- split-KV paged decode attention over the FP4 cache
+ * (ultraquant_attn, UltraQuantAttentionImpl._decode_attention;
+ * flydsl_ultraquant_decode, flydsl_ultraquant_decode_attention).
+ *
+ *   query        bf16, element (b, r, d) at b * q_stride_seq +
+ *                r * q_stride_head + d (elements; 16-byte aligned rows).
+ *   kv_cache     uint8 cache written by uq_store (read only).
+ *   block_table  int32 [B][max_blocks_per_seq]: page ids of each sequence.
+ *   seq_lens     int32 [B]: tokens of each sequence, 0 <= L <=
+ *                max_blocks_per_seq * block_size (larger values are clamped
+ *                to that capacity on the device).
+ *   scale        softmax scale applied to q'.k (typically 1/sqrt(D)).
+ *   max_num_kv_splits  S, the fixed number of splits per (sequence, kv head);
+ *                1 <= S <= 256.  The grid depends only on (S, Hk, B), so the
+ *                call can be captured once in a CUDA graph and replayed with
+ *                new seq_lens / block_table contents.
+ *   workspace    device scratch of at least
+ *                uq_decode_workspace_bytes(B, Hq, D, S) bytes, 256-byte
+ *                aligned; contents need no initialisation.
+ *   out          bf16 [B][Hq][D] contiguous, written.
+ *
+ * Per query head r (kv head r / (Hq/Hk)): q' = bf16(e4m3(fp32(q) H)) (the
+ * E4M3 "haircut", round to nearest even, saturating); s_t = scale * q'.k_t
+ * over the L tokens of the sequence, k_t the dequantised rotated K;
+ * out = softmax(s) . V (dequantised), rounded to bf16.  A sequence with
+ * L == 0 gets out = 0.  Tokens are divided into up to S splits of whole
+ * pages; each split's partial output and log-sum-exp are merged by a second
+ * kernel on the same stream.
+ */
+uq_status uq_decode(const void *query, const void *kv_cache,
+                    const int32_t *block_table, const int32_t *seq_lens,
+                    float scale, int max_num_kv_splits, void *workspace,
+                    size_t workspace_bytes, void *out, int B, int Hq, int Hk,
+                    int head_dim, int num_blocks, int block_size,
+                    int max_blocks_per_seq, int slot_bytes, int64_t q_stride_seq,
+                    int64_t q_stride_head, void *stream);
+
+/*
+ * Profiling hook.  When set (non-NULL), the next uq_decode calls made by the
+ * calling thread record `before_stage1` on their stream just before the
+ * stage-1 kernel and `after_stage1` just after it, so a caller can time the
+ * split-KV kernel alone with cudaEventElapsedTime.  Both are cudaEvent_t
+ * handles passed as void*, owned by the caller; NULL, NULL turns it off.
+ * Recording is part of the enqueued work, so it is captured into a CUDA
+ * graph like the kernels.  Always returns UQ_OK.
+ */
+uq_status uq_set_timing_events(void *before_stage1, void *after_stage1);
+
+/* Message describing the last error returned on the calling thread ("" if none). */
+const char *uq_last_error(void);
+
+/*
+ * Synchronise `stream`, read and clear the device error word of the current
+ * device.  Returns UQ_OK if no bit was set, UQ_ERR_DEVICE_FLAG (bits in
+ * *flags_out when non-NULL) if any was, UQ_ERR_CUDA on a runtime error.
+ * Intended for tests and debugging, outside the hot path.
+ */
+uq_status uq_check_device_error(void *stream, unsigned int *flags_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* UQ_H */
