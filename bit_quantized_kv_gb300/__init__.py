@@ -13,7 +13,7 @@ from __future__ import annotations
 
 _API = ("uq_store", "uq_store_rotated_f32", "uq_decode", "uq_decode_workspace_bytes",
         "uq_slot_bytes", "uq_check_device_error", "uq_last_error", "uq_version",
-        "uq_set_timing_events", "UQError")
+        "uq_set_timing_events", "uq_decode_static_scratch", "UQError")
 
 __all__ = list(_API)
 

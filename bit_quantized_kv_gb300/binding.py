@@ -32,8 +32,8 @@ HEAD_DIM = 256
 SLOT_BYTES = 272
 
 EXPORTED = ("uq_version", "uq_slot_bytes", "uq_decode_workspace_bytes", "uq_store",
-            "uq_store_rotated_f32", "uq_decode", "uq_set_timing_events", "uq_last_error",
-            "uq_check_device_error")
+            "uq_store_rotated_f32", "uq_decode", "uq_decode_static_scratch",
+            "uq_set_timing_events", "uq_last_error", "uq_check_device_error")
 
 
 class UQError(RuntimeError):
@@ -70,6 +70,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.uq_decode.restype = c_int
     L.uq_decode.argtypes = [c_p, c_p, c_p, c_p, c_f, c_int, c_p, c_sz, c_p, c_int, c_int,
                             c_int, c_int, c_int, c_int, c_int, c_int, c_i64, c_i64, c_p]
+    L.uq_decode_static_scratch.restype = c_int
+    L.uq_decode_static_scratch.argtypes = [c_p, c_p, c_p, c_p, c_f, c_int, c_p, c_int, c_int,
+                                           c_int, c_int, c_int, c_int, c_int, c_int, c_i64,
+                                           c_i64, c_p]
     L.uq_set_timing_events.restype = c_int
     L.uq_set_timing_events.argtypes = [c_p, c_p]
     L.uq_last_error.restype = ctypes.c_char_p
@@ -189,6 +193,30 @@ def uq_decode(query: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Te
                             workspace.data_ptr(), ws_bytes, out.data_ptr(), B, Hq, Hk, D,
                             nb, bs, block_table.shape[1], sb, query.stride(0), query.stride(1),
                             _stream_ptr(stream)))
+    return out
+
+
+def uq_decode_static_scratch(query: torch.Tensor, kv_cache: torch.Tensor,
+                             block_table: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                             max_num_kv_splits: int, out: torch.Tensor, stream=None) -> torch.Tensor:
+    """uq_decode without a workspace argument, for callers that cannot
+    allocate device memory: the split partials go to the library's fixed
+    32 MiB scratch (B * Hq * max_num_kv_splits <= 32640).  Calls that may run
+    concurrently on the GPU share that scratch and must not overlap."""
+    _need(query, "query", torch.bfloat16, 3)
+    _need(kv_cache, "kv_cache", torch.uint8, 4)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(out, "out", torch.bfloat16, 3)
+    B, Hq, D = query.shape
+    if query.stride(2) != 1 or out.shape != query.shape or not out.is_contiguous():
+        raise ValueError("query rows must be contiguous and out shaped like query")
+    nb, bs, Hk, sb = kv_cache.shape
+    _check(load().uq_decode_static_scratch(query.data_ptr(), kv_cache.data_ptr(),
+                                           block_table.data_ptr(), seq_lens.data_ptr(),
+                                           float(scale), int(max_num_kv_splits), out.data_ptr(),
+                                           B, Hq, Hk, D, nb, bs, block_table.shape[1], sb,
+                                           query.stride(0), query.stride(1), _stream_ptr(stream)))
     return out
 
 

@@ -95,6 +95,11 @@ uq_status check_store_args(const void* key, const void* value, void* kv_cache,
 
 }  // namespace
 
+namespace uq {
+// Records an error message for uq_last_error() from another translation unit.
+uq_status set_error(uq_status code, const char* msg) { return fail(code, "%s", msg); }
+}  // namespace uq
+
 extern "C" {
 
 int uq_version(void) { return kVersion; }

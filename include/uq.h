@@ -167,6 +167,35 @@ uq_status uq_decode(const void *query, const void *kv_cache,
                     int64_t q_stride_head, void *stream);
 
 /*
+ * uq_decode_static_scratch -- uq_decode for callers that cannot allocate
+ * device memory.  The paper has no counterpart; this entry point exists for
+ * integrations where nobody can hand uq_decode a workspace: for example a
+ * plugin whose enqueue step must not call cudaMalloc (the call can
+ * synchronise the device and can fail in the middle of serving), or a host
+ * that keeps all device memory in its own pool and gives its kernels no
+ * allocator.  It runs exactly uq_decode, with the split partials in a scratch
+ * array of 32 MiB that the library declares statically: every GPU that loads
+ * this library holds that array until the process exits.
+ *
+ * Arguments are those of uq_decode without workspace and workspace_bytes.
+ * A batch whose uq_decode_workspace_bytes(B, Hq, 256, max_num_kv_splits)
+ * exceeds 32 MiB (B * Hq * max_num_kv_splits > 32640) is rejected with
+ * UQ_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.  The call allocates
+ * nothing.  The first call on a device looks up the array's device address;
+ * make that first call before any stream capture.  All calls on a device
+ * share the one array, and it keeps the previous call's partials (nothing in
+ * it needs to start at zero), so calls that can overlap on the GPU (for
+ * example on two streams without an ordering between them) race.
+ */
+uq_status uq_decode_static_scratch(const void *query, const void *kv_cache,
+                                   const int32_t *block_table, const int32_t *seq_lens,
+                                   float scale, int max_num_kv_splits, void *out, int B,
+                                   int Hq, int Hk, int head_dim, int num_blocks,
+                                   int block_size, int max_blocks_per_seq, int slot_bytes,
+                                   int64_t q_stride_seq, int64_t q_stride_head,
+                                   void *stream);
+
+/*
  * Profiling hook.  When set (non-NULL), the next uq_decode calls made by the
  * calling thread record `before_stage1` on their stream just before the
  * stage-1 kernel and `after_stage1` just after it, so a caller can time the
