@@ -503,6 +503,17 @@ decode_stage2(const float* __restrict__ part_o, const float* __restrict__ part_l
   *reinterpret_cast<uint4*>(out + (int64_t)row * kHeadDim + lane * 8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
 }
 
+// Record a caller's timing event.  Under stream capture a plain record only
+// becomes a dependency edge, so it is captured as an external event node.
+static cudaError_t record_timing_event(cudaEvent_t ev, cudaStream_t stream) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+  if (e != cudaSuccess) return e;
+  return cs == cudaStreamCaptureStatusActive
+             ? cudaEventRecordWithFlags(ev, stream, cudaEventRecordExternal)
+             : cudaEventRecord(ev, stream);
+}
+
 template <int NT>
 static cudaError_t launch_stage1_t(const uint16_t* query, int64_t q_ss, int64_t q_sh,
                                    const uint8_t* kv, const int32_t* bt, const int32_t* sl,
@@ -536,7 +547,7 @@ cudaError_t launch_decode(const uint16_t* query, int64_t q_ss, int64_t q_sh, con
   float* part_lse = part_o + (size_t)B * Hq * S * kHeadDim;
   const int QG = Hq / Hk;
   if (ev_before_stage1) {
-    cudaError_t er = cudaEventRecord(ev_before_stage1, stream);
+    cudaError_t er = record_timing_event(ev_before_stage1, stream);
     if (er != cudaSuccess) return er;
   }
   cudaError_t e = (QG == 16)
@@ -544,7 +555,7 @@ cudaError_t launch_decode(const uint16_t* query, int64_t q_ss, int64_t q_sh, con
       : launch_stage1_t<1>(query, q_ss, q_sh, kv, bt, sl, scale, B, Hq, Hk, num_blocks, max_blocks, S, part_o, part_lse, err, stream);
   if (e != cudaSuccess) return e;
   if (ev_after_stage1) {
-    e = cudaEventRecord(ev_after_stage1, stream);
+    e = record_timing_event(ev_after_stage1, stream);
     if (e != cudaSuccess) return e;
   }
   const int rows = B * Hq;
