@@ -201,7 +201,7 @@ def uq_decode_static_scratch(query: torch.Tensor, kv_cache: torch.Tensor,
                              max_num_kv_splits: int, out: torch.Tensor, stream=None) -> torch.Tensor:
     """uq_decode without a workspace argument, for callers that cannot
     allocate device memory: the split partials go to the library's fixed
-    32 MiB scratch (B * Hq * max_num_kv_splits <= 32640).  Calls that may run
+    32 MiB scratch (roughly B * Hq * max_num_kv_splits <= 32480).  Calls that may run
     concurrently on the GPU share that scratch and must not overlap."""
     _need(query, "query", torch.bfloat16, 3)
     _need(kv_cache, "kv_cache", torch.uint8, 4)

@@ -23,6 +23,7 @@ cudaError_t launch_decode(const uint16_t* query, int64_t q_ss, int64_t q_sh, con
                           int Hk, int num_blocks, int max_blocks, int S, void* workspace,
                           uint16_t* out, unsigned* err, cudaStream_t stream,
                           cudaEvent_t ev_before_stage1, cudaEvent_t ev_after_stage1);
+size_t decode_workspace_bytes(int B, int Hq, int S);
 }  // namespace uq
 
 namespace {
@@ -109,11 +110,9 @@ size_t uq_slot_bytes(int head_dim) {
 }
 
 size_t uq_decode_workspace_bytes(int B, int Hq, int head_dim, int max_num_kv_splits) {
-  if (B < 0 || Hq < 1 || head_dim != uq::kHeadDim || max_num_kv_splits < 1 || max_num_kv_splits > 256)
+  if (B < 1 || Hq < 1 || head_dim != uq::kHeadDim || max_num_kv_splits < 1 || max_num_kv_splits > 256)
     return 0;
-  const size_t rows = (size_t)B * Hq * max_num_kv_splits;
-  const size_t bytes = rows * (head_dim + 1) * sizeof(float);
-  return (bytes + 255) / 256 * 256;
+  return uq::decode_workspace_bytes(B, Hq, max_num_kv_splits);
 }
 
 const char* uq_last_error(void) { return g_last_error; }
@@ -179,7 +178,10 @@ uq_status uq_decode(const void* query, const void* kv_cache, const int32_t* bloc
     return fail(UQ_ERR_INVALID_ARG, "max_num_kv_splits %d outside [1, 256]", max_num_kv_splits);
   if (num_blocks < 1 || max_blocks_per_seq < 1)
     return fail(UQ_ERR_INVALID_ARG, "num_blocks %d / max_blocks_per_seq %d must be >= 1", num_blocks, max_blocks_per_seq);
-  if (B > 65535 || Hk > 65535) return fail(UQ_ERR_INVALID_ARG, "B %d or Hk %d exceeds the grid limit 65535", B, Hk);
+  if (B > 65535) return fail(UQ_ERR_INVALID_ARG, "B %d exceeds 65535", B);
+  if (Hk > 256) return fail(UQ_ERR_UNSUPPORTED, "Hk %d exceeds 256", Hk);
+  if ((int64_t)B * Hq * max_num_kv_splits > ((int64_t)1 << 30))
+    return fail(UQ_ERR_INVALID_ARG, "B * Hq * max_num_kv_splits exceeds 2^30");
   if (!(scale == scale)) return fail(UQ_ERR_INVALID_ARG, "scale is NaN");
   if (B == 0) return ok();
   if (!query || !kv_cache || !block_table || !seq_lens || !workspace || !out)

@@ -4,13 +4,23 @@
 // stage-1 split partials, partition reduce; the fixed split count follows
 // vllm.v1.attention.ops.turboquant_soa.triton_turboquant_decode_v2).
 //
-// Stage 1: one CTA per (split, kv head, sequence), 4 warps.  A split is a run
-// of whole 16-token pages; each warp takes every 4th page of it and keeps its
-// own online-softmax state.  A page's 16 slots of one kv head (16 x 272 B)
-// are brought into shared memory by bulk async copies that complete on a
-// per-stage mbarrier, NSTAGE pages ahead.  The CTA's query group (6, 8 or 16
-// rows) is rotated once (fp32 butterfly, x 1/16), rounded through E4M3, and
-// kept as f16 tensor-core fragments.
+// Three kernels on the caller's stream:
+//
+// Plan (one CTA).  Reads seq_lens and chooses, for the whole batch, one unit
+// size T (pages of one kv head) so that the batch splits into about
+// kUnitsPerCta work units per resident stage-1 CTA, never below
+// kMinPagesPerUnit pages.  Sequence b gets n_b = min(S, ceil(P_b / T)) splits
+// of whole pages.  Units (sequence, split, kv head) are listed with the
+// longest units first; the plan also resets the unit counter.
+//
+// Stage 1 (persistent: resident CTAs only, 4 warps each).  Each CTA takes
+// units from the counter.  Inside a unit each warp takes every 4th page and
+// keeps its own online-softmax state; a page's 16 slots of one kv head
+// (16 x 272 B) arrive in shared memory by bulk async copies completing on a
+// per-stage mbarrier, NSTAGE pages ahead.  The unit's query group (6, 8 or 16
+// rows) is rotated (fp32 butterfly, x 1/16), rounded through E4M3 and kept
+// in shared memory as f16 in tensor-core operand order.  At the end of the
+// unit the four warps' states are merged into one split partial.
 //
 // Tensor-core formulation (mma.m16n8k16, f16 in, fp32 accumulate):
 //   QK:  S[t, r] = sum_d K'[t, d] Q'[r, d]      (M = 16 tokens, N = 8 rows)
@@ -34,23 +44,59 @@ namespace uq {
 
 constexpr int kPage = 16;                        // tokens per page (block_size)
 constexpr int kTileBytes = kPage * kSlotBytes;   // 4352 bytes per (page, kv head)
-constexpr int kMinPagesPerSplit = 8;             // floor of 128 tokens per split
+#ifndef UQ_MIN_PAGES_PER_UNIT
+#define UQ_MIN_PAGES_PER_UNIT 8
+#endif
+#ifndef UQ_UNITS_PER_CTA
+#define UQ_UNITS_PER_CTA 4
+#endif
+#ifndef UQ_S1_NSTAGE
+#define UQ_S1_NSTAGE 3
+#endif
+#ifndef UQ_S1_MIN_BLOCKS
+#define UQ_S1_MIN_BLOCKS 3
+#endif
+constexpr int kMinPagesPerUnit = UQ_MIN_PAGES_PER_UNIT;  // floor of 128 tokens per split
+constexpr int kUnitsPerCta = UQ_UNITS_PER_CTA;           // work units per resident CTA
+constexpr int kStage1Stages = UQ_S1_NSTAGE;              // pages in flight per warp
+constexpr int kPlanThreads = 1024;
 constexpr float kLog2e = 1.4426950408889634f;
 
-struct SplitPlan {
-  int pages_per_split;
-  int n_active;
+// ---------------------------------------------------------------------------
+// Workspace layout (caller-owned, no initialisation needed).
+// ---------------------------------------------------------------------------
+struct Workspace {
+  float* part_o;       // [B][Hq][S][256] split outputs, normalised
+  float* part_lse;     // [B][Hq][S]      log2-sum-exp of each split
+  uint32_t* units;     // [<= S * B * Hk] b | split << 16 | kv_head << 24
+  int2* seq_info;      // [B] (pages per split, active splits)
+  int* order;          // [B] sequences with at least one page, longest split first
+  int* hdr;            // [0] number of units, [1] next unit to take
 };
 
-// Split assignment, identical in both stages: up to S splits of whole pages,
-// each at least kMinPagesPerSplit pages unless the sequence is shorter.
-__device__ __forceinline__ SplitPlan split_plan(int L, int S) {
-  const int P = (L + kPage - 1) / kPage;
-  if (P <= 0) return {0, 0};
-  const int want = (P + kMinPagesPerSplit - 1) / kMinPagesPerSplit;
-  const int ns = min(S, max(1, want));
-  const int pps = (P + ns - 1) / ns;
-  return {pps, (P + pps - 1) / pps};
+__host__ __device__ inline size_t workspace_bytes(int B, int Hq, int S) {
+  const size_t rows = (size_t)B * Hq * S;
+  const size_t bytes = rows * kHeadDim * 4 + rows * 4 + rows * 4 + (size_t)B * 8 +
+                       (size_t)B * 4 + 64;
+  return (bytes + 255) / 256 * 256;
+}
+
+__host__ __device__ inline Workspace workspace_layout(void* base, int B, int Hq, int S) {
+  const size_t rows = (size_t)B * Hq * S;
+  uint8_t* p = static_cast<uint8_t*>(base);
+  Workspace w;
+  w.part_o = reinterpret_cast<float*>(p);
+  p += rows * kHeadDim * 4;
+  w.part_lse = reinterpret_cast<float*>(p);
+  p += rows * 4;
+  w.units = reinterpret_cast<uint32_t*>(p);
+  p += rows * 4;
+  w.seq_info = reinterpret_cast<int2*>(p);   // rows * 1032 is a multiple of 8
+  p += (size_t)B * 8;
+  w.order = reinterpret_cast<int*>(p);
+  p += (size_t)B * 4;
+  w.hdr = reinterpret_cast<int*>(p);
+  return w;
 }
 
 __device__ __forceinline__ int clamp_len(int L, int max_blocks) {
@@ -59,6 +105,103 @@ __device__ __forceinline__ int clamp_len(int L, int max_blocks) {
   return (long long)L > cap ? (int)cap : L;
 }
 
+// ---------------------------------------------------------------------------
+// Plan.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kPlanThreads)
+decode_plan(const int32_t* __restrict__ seq_lens, int B, int Hk, int S, int max_blocks,
+            int target_units, Workspace ws) {
+  __shared__ long long s_part[kPlanThreads / 32];
+  __shared__ int s_hist[32], s_cursor[32], s_wsum[kPlanThreads / 32];
+  __shared__ long long s_total;
+  __shared__ int s_nseq;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid < 32) s_hist[tid] = 0;
+
+  long long mine = 0;
+  for (int b = tid; b < B; b += kPlanThreads) mine += (clamp_len(seq_lens[b], max_blocks) + kPage - 1) / kPage;
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, m);
+  if (lane == 0) s_part[warp] = mine;
+  __syncthreads();
+  if (tid == 0) {
+    long long t = 0;
+    for (int w = 0; w < kPlanThreads / 32; ++w) t += s_part[w];
+    s_total = t;
+  }
+  __syncthreads();
+  const long long work = s_total * Hk;
+  long long T = (work + target_units - 1) / max(target_units, 1);
+  if (T < kMinPagesPerUnit) T = kMinPagesPerUnit;
+
+  for (int b = tid; b < B; b += kPlanThreads) {
+    const int P = (clamp_len(seq_lens[b], max_blocks) + kPage - 1) / kPage;
+    int n = 0, pps = 0, nact = 0;
+    if (P > 0) {
+      const long long want = (P + T - 1) / T;
+      n = (int)(want < S ? want : S);
+      n = max(n, 1);
+      pps = (P + n - 1) / n;
+      nact = (P + pps - 1) / pps;
+      atomicAdd(&s_hist[31 - __clz(pps)], 1);
+    }
+    ws.seq_info[b] = make_int2(pps, nact);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int acc = 0;
+    for (int k = 31; k >= 0; --k) {   // longest splits first
+      s_cursor[k] = acc;
+      acc += s_hist[k];
+    }
+    s_nseq = acc;
+  }
+  __syncthreads();
+  for (int b = tid; b < B; b += kPlanThreads) {
+    const int pps = ws.seq_info[b].x;
+    if (pps > 0) ws.order[atomicAdd(&s_cursor[31 - __clz(pps)], 1)] = b;
+  }
+  __syncthreads();
+
+  // units: exclusive prefix over the ordered sequences of (active splits * Hk)
+  const int nseq = s_nseq;
+  const int chunk = (nseq + kPlanThreads - 1) / kPlanThreads;
+  const int lo = min(nseq, tid * chunk), hi = min(nseq, lo + chunk);
+  int cnt = 0;
+  for (int k = lo; k < hi; ++k) cnt += ws.seq_info[ws.order[k]].y * Hk;
+  int incl = cnt;
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, m);
+    if (lane >= m) incl += v;
+  }
+  if (lane == 31) s_wsum[warp] = incl;
+  __syncthreads();
+  if (tid == 0) {
+    int acc = 0;
+    for (int w = 0; w < kPlanThreads / 32; ++w) {
+      const int t = s_wsum[w];
+      s_wsum[w] = acc;
+      acc += t;
+    }
+  }
+  __syncthreads();
+  int off = s_wsum[warp] + incl - cnt;
+  for (int k = lo; k < hi; ++k) {
+    const int b = ws.order[k];
+    const int nact = ws.seq_info[b].y;
+    for (int s = 0; s < nact; ++s)
+      for (int g = 0; g < Hk; ++g) ws.units[off++] = (uint32_t)b | ((uint32_t)s << 16) | ((uint32_t)g << 24);
+  }
+  if (tid == kPlanThreads - 1) {
+    ws.hdr[0] = off;   // the last thread's range ends the list
+    ws.hdr[1] = 0;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Stage 1.
+// ---------------------------------------------------------------------------
 template <int NT, int NWARPS, int NSTAGE>
 struct Stage1Layout {
   static constexpr int kRows = NT * 8;                       // padded query rows
@@ -70,315 +213,175 @@ struct Stage1Layout {
   static constexpr int kStatsBytes = NWARPS * kRows * 4 * 4;
   static constexpr int kRowInfoOff = kStatsOff + kStatsBytes; // [kRows][NWARPS+2] floats
   static constexpr int kRowInfoBytes = kRows * (NWARPS + 2) * 4;
-  static constexpr int kBarOff = (kRowInfoOff + kRowInfoBytes + 15) / 16 * 16;
+  static constexpr int kLutOff = (kRowInfoOff + kRowInfoBytes + 15) / 16 * 16;
+  static constexpr int kLutBytes = 256 * 4;                  // 2^-delta as f16x2
+  // per warp, per tile: [K, V][token] 8 relative block scales (f16) and one factor
+  static constexpr int kMetaRelBytes = 2 * kPage * 16;
+  static constexpr int kMetaWarpBytes = kMetaRelBytes + 2 * kPage * 4;
+  static constexpr int kMetaOff = kLutOff + kLutBytes;
+  static constexpr int kBarOff = kMetaOff + NWARPS * kMetaWarpBytes;
   static constexpr int kBarBytes = NWARPS * NSTAGE * 8;
-  static constexpr int kQOff = (kBarOff + kBarBytes + 127) / 128 * 128;
-  static constexpr int kQBytes = kRows * kHeadDim * 2;      // f16 [kRows][256]
+  static constexpr int kMiscOff = kBarOff + kBarBytes;       // unit id, abort flag
+  static constexpr int kQOff = (kMiscOff + 16 + 127) / 128 * 128;
+  static constexpr int kQRowBytes = kHeadDim * 2 + 16;       // padded: conflict-free ldmatrix
+  static constexpr int kQBytes = kRows * kQRowBytes;
   static constexpr int kBytes = kQOff + kQBytes;
 };
 
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                            uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+
 template <int NT, int NWARPS, int NSTAGE>
-__global__ void __launch_bounds__(NWARPS * 32, NT == 1 ? 3 : 2)
+__global__ void __launch_bounds__(NWARPS * 32, NT == 1 ? UQ_S1_MIN_BLOCKS : 2)
 decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
               const uint8_t* __restrict__ kv, const int32_t* __restrict__ block_table,
               const int32_t* __restrict__ seq_lens, float scale_log2e, int Hq, int Hk,
-              int QG, int num_blocks, int max_blocks, int S, float* __restrict__ part_o,
-              float* __restrict__ part_lse, unsigned* __restrict__ err) {
+              int QG, int num_blocks, int max_blocks, int S, Workspace ws,
+              unsigned* __restrict__ err) {
   using Lay = Stage1Layout<NT, NWARPS, NSTAGE>;
-  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-  const int L = clamp_len(seq_lens[b], max_blocks);
-  const SplitPlan plan = split_plan(L, S);
-  if (split >= plan.n_active) return;
-  const int P = (L + kPage - 1) / kPage;
-  const int p_begin = split * plan.pages_per_split;
-  const int p_end = min(p_begin + plan.pages_per_split, P);
-
+  constexpr int NCH = NT == 1 ? 4 : 2;   // independent QK accumulator chains per n-tile
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, c = lane & 3;
   const uint32_t smem_base = smem_u32(smem);
   const uint32_t bar_base = smem_base + Lay::kBarOff + warp * NSTAGE * 8;
   const uint32_t stage_base = smem_base + warp * NSTAGE * kTileBytes;
+  const uint32_t lut_base = smem_base + Lay::kLutOff;
+  const uint32_t meta_rel = smem_base + Lay::kMetaOff + warp * Lay::kMetaWarpBytes;
+  const uint32_t meta_f = meta_rel + Lay::kMetaRelBytes;
+  volatile int* s_misc = reinterpret_cast<volatile int*>(smem + Lay::kMiscOff);
+  uint16_t* qs = reinterpret_cast<uint16_t*>(smem + Lay::kQOff);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NWARPS * NSTAGE; ++i) mbar_init(smem_base + Lay::kBarOff + 8 * i, 1);
+    s_misc[1] = 0;
     fence_barrier_init();
   }
-  __syncthreads();
-
-  // ---- per-warp page schedule -------------------------------------------
-  const int n_pages = p_end - p_begin;
-  const int n_my = n_pages > warp ? (n_pages - warp + NWARPS - 1) / NWARPS : 0;
-  const int32_t* bt_row = block_table + (int64_t)b * max_blocks + p_begin + warp;
-  int pid_chunk = -1, pid_reg = -1;
-  uint32_t stage_ok = 0;  // bit s: stage s holds a page that was really copied
-
-  auto issue = [&](int j) {
-    const int chunk = j >> 5;
-    if (chunk != pid_chunk) {
-      const int jj = chunk * 32 + lane;
-      pid_reg = jj < n_my ? bt_row[(int64_t)jj * NWARPS] : -1;
-      pid_chunk = chunk;
-    }
-    const int pid = __shfl_sync(0xffffffffu, pid_reg, j & 31);
-    const int stg = j % NSTAGE;
-    const uint32_t bar = bar_base + 8 * stg;
-    const bool ok = (unsigned)pid < (unsigned)num_blocks;
-    stage_ok = ok ? (stage_ok | (1u << stg)) : (stage_ok & ~(1u << stg));
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      if (ok) {
-        mbar_arrive_expect_tx(bar, kTileBytes);
-      } else {
-        atomicOr(err, kErrBadPage);
-        mbar_arrive(bar);
-      }
-    }
-    __syncwarp();
-    if (ok && lane < kPage) {
-      const uint8_t* src = kv + (((int64_t)pid * kPage + lane) * Hk + g) * (int64_t)kSlotBytes;
-      bulk_g2s(stage_base + stg * kTileBytes + lane * kSlotBytes, src, kSlotBytes, bar);
-    }
-  };
-
-  for (int j = 0; j < NSTAGE && j < n_my; ++j) issue(j);
-
-  // ---- query prologue: q' = f16(e4m3(fp32(q) H)) --------------------------
-  uint16_t* qs = reinterpret_cast<uint16_t*>(smem + Lay::kQOff);
-  for (int r = warp; r < Lay::kRows; r += NWARPS) {
-    uint4 packed = make_uint4(0, 0, 0, 0);
-    if (r < QG) {
-      const uint16_t* qp = query + (int64_t)b * q_ss + (int64_t)(g * QG + r) * q_sh + lane * 8;
-      const uint4 raw = *reinterpret_cast<const uint4*>(qp);
-      float x[8];
-      const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        x[2 * i] = bf16_bits_to_f32(u[i] & 0xffffu);
-        x[2 * i + 1] = bf16_bits_to_f32(u[i] >> 16);
-      }
-#pragma unroll
-      for (int h = 1; h < 8; h <<= 1)
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if ((i & h) == 0) {
-            const float a = x[i], c = x[i + h];
-            x[i] = a + c;
-            x[i + h] = a - c;
-          }
-#pragma unroll
-      for (int m = 1; m < 32; m <<= 1) {
-        const bool upper = (lane & m) != 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float other = __shfl_xor_sync(0xffffffffu, x[i], m);
-          x[i] = upper ? (other - x[i]) : (x[i] + other);
-        }
-      }
-      packed.x = e4m3_roundtrip_f16x2(x[0] * 0.0625f, x[1] * 0.0625f);
-      packed.y = e4m3_roundtrip_f16x2(x[2] * 0.0625f, x[3] * 0.0625f);
-      packed.z = e4m3_roundtrip_f16x2(x[4] * 0.0625f, x[5] * 0.0625f);
-      packed.w = e4m3_roundtrip_f16x2(x[6] * 0.0625f, x[7] * 0.0625f);
-    }
-    *reinterpret_cast<uint4*>(qs + r * kHeadDim + lane * 8) = packed;
+  for (int i = threadIdx.x; i < 256; i += NWARPS * 32) {
+    const uint32_t h = pow2_neg_f16(i);
+    reinterpret_cast<uint32_t*>(smem + Lay::kLutOff)[i] = h | (h << 16);
   }
   __syncthreads();
 
-  const int gq = lane >> 2, c = lane & 3;
-  // Q' B-fragments: k-step i, lane (gq, c): row 8nt+gq, head dims 64c+4i .. +3
-  uint32_t qf[NT][16][2];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const uint32_t base = smem_u32(qs + (nt * 8 + gq) * kHeadDim + 64 * c);
-#pragma unroll
-    for (int i2 = 0; i2 < 8; ++i2) {
-      const uint4 v = lds128(base + 16 * i2);
-      qf[nt][2 * i2][0] = v.x;
-      qf[nt][2 * i2][1] = v.y;
-      qf[nt][2 * i2 + 1][0] = v.z;
-      qf[nt][2 * i2 + 1][1] = v.w;
-    }
-  }
-
-  // ---- main loop ------------------------------------------------------------
-  float o[NT][16][4];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int mt = 0; mt < 16; ++mt) o[nt][mt][0] = o[nt][mt][1] = o[nt][mt][2] = o[nt][mt][3] = 0.f;
-  float m_run[NT][2], mu_run[NT][2], l_run[NT][2];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      m_run[nt][h] = -INFINITY;
-      mu_run[nt][h] = -INFINITY;
-      l_run[nt][h] = 0.f;
-    }
-
+  const int n_units = ws.hdr[0];
+  uint32_t tiles_done = 0;   // this warp's tiles so far: drives stage and parity
+  uint32_t stage_ok = 0;     // bit s: stage s holds a page that was really copied
   const int ta = 2 * c, tb = 2 * c + 1, tcc = 2 * c + 8, td = 2 * c + 9;
-  bool timed_out = false;
-  int j = 0;
-  for (; j < n_my; ++j) {
-    const int stg = j % NSTAGE;
-    if (!mbar_wait(bar_base + 8 * stg, (uint32_t)((j / NSTAGE) & 1))) {
-      timed_out = true;
-      break;
-    }
-    const int page = p_begin + warp + j * NWARPS;
-    const int nvalid = ((stage_ok >> stg) & 1u) ? min(kPage, L - page * kPage) : 0;
-    if (nvalid > 0) {
-      const uint32_t sb = stage_base + stg * kTileBytes;
-      // -- K scales of tokens gq, gq+8: token max E and the relative scales of
-      //    blocks 2c, 2c+1 as f16x2 (both halves equal)
-      const uint2 ks0 = lds64(sb + gq * kSlotBytes + kKScaleOff);
-      const uint2 ks1 = lds64(sb + (gq + 8) * kSlotBytes + kKScaleOff);
-      const uint32_t ek0 = max_byte8(ks0.x, ks0.y), ek1 = max_byte8(ks1.x, ks1.y);
-      const uint32_t kw0 = (c < 2) ? ks0.x : ks0.y, kw1 = (c < 2) ? ks1.x : ks1.y;
-      const int sh = 16 * (c & 1);
-      uint32_t rk0[2], rk1[2];
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const uint32_t h0 = pow2_neg_f16((int)ek0 - (int)((kw0 >> (sh + 8 * q)) & 0xffu));
-        const uint32_t h1 = pow2_neg_f16((int)ek1 - (int)((kw1 >> (sh + 8 * q)) & 0xffu));
-        rk0[q] = h0 | (h0 << 16);
-        rk1[q] = h1 | (h1 << 16);
-      }
-      // -- QK on the tensor cores
-      const uint4 ka0 = lds128(sb + gq * kSlotBytes + 32 * c);
-      const uint4 ka1 = lds128(sb + gq * kSlotBytes + 32 * c + 16);
-      const uint4 kb0 = lds128(sb + (gq + 8) * kSlotBytes + 32 * c);
-      const uint4 kb1 = lds128(sb + (gq + 8) * kSlotBytes + 32 * c + 16);
-      const uint32_t kaw[8] = {ka0.x, ka0.y, ka0.z, ka0.w, ka1.x, ka1.y, ka1.z, ka1.w};
-      const uint32_t kbw[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
-      float sacc[NT][4];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        uint32_t fa[4], fb[4];
-        f16x2x4_from_e2m1_word(kaw[q], fa);
-        f16x2x4_from_e2m1_word(kbw[q], fb);
-        const uint32_t ra = rk0[q >> 2], rb = rk1[q >> 2];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          fa[e] = hmul2(fa[e], ra);
-          fb[e] = hmul2(fb[e], rb);
-        }
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const int i = 2 * q + half;
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-            mma_f16_16816(sacc[nt], fa[2 * half], fb[2 * half], fa[2 * half + 1],
-                          fb[2 * half + 1], qf[nt][i][0], qf[nt][i][1]);
-        }
-      }
-      // -- V scales: tokens 2c, 2c+1, 2c+8, 2c+9 (E and block gq byte)
-      const uint2 vsa = lds64(sb + ta * kSlotBytes + kVScaleOff);
-      const uint2 vsb = lds64(sb + tb * kSlotBytes + kVScaleOff);
-      const uint2 vsc = lds64(sb + tcc * kSlotBytes + kVScaleOff);
-      const uint2 vsd = lds64(sb + td * kSlotBytes + kVScaleOff);
-      const uint32_t eva = max_byte8(vsa.x, vsa.y), evb = max_byte8(vsb.x, vsb.y);
-      const uint32_t evc = max_byte8(vsc.x, vsc.y), evd = max_byte8(vsd.x, vsd.y);
-      const int bsh = 8 * (gq & 3);
-      const uint32_t bya = (((gq < 4) ? vsa.x : vsa.y) >> bsh) & 0xffu;
-      const uint32_t byb = (((gq < 4) ? vsb.x : vsb.y) >> bsh) & 0xffu;
-      const uint32_t byc = (((gq < 4) ? vsc.x : vsc.y) >> bsh) & 0xffu;
-      const uint32_t byd = (((gq < 4) ? vsd.x : vsd.y) >> bsh) & 0xffu;
-      const uint32_t rv01 = pow2_neg_f16((int)eva - (int)bya) | (pow2_neg_f16((int)evb - (int)byb) << 16);
-      const uint32_t rv89 = pow2_neg_f16((int)evc - (int)byc) | (pow2_neg_f16((int)evd - (int)byd) << 16);
-      // V exponents of tokens gq and gq+8 come from lane c' = gq / 2
-      const uint32_t evpack = eva | (evb << 8) | (evc << 16) | (evd << 24);
-      const uint32_t evsrc = __shfl_sync(0xffffffffu, evpack, gq >> 1);
-      const int ev0 = (int)((evsrc >> (8 * (gq & 1))) & 0xffu);
-      const int ev1 = (int)((evsrc >> (16 + 8 * (gq & 1))) & 0xffu);
 
-      // -- scores and online softmax
-      const float fk0 = scale_log2e * ue8m0_to_f32(ek0);
-      const float fk1 = scale_log2e * ue8m0_to_f32(ek1);
-      const bool v0 = gq < nvalid, v1 = gq + 8 < nvalid;
-      uint32_t pw[NT][2];
-      bool rescale = false;
-      float alpha_o[NT][2];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        float w4[4];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const float s0 = v0 ? sacc[nt][h] * fk0 : -INFINITY;
-          const float s1 = v1 ? sacc[nt][2 + h] * fk1 : -INFINITY;
-          const float u0 = s0 + (float)(ev0 - 127);
-          const float u1 = s1 + (float)(ev1 - 127);
-          float tmax = fmaxf(s0, s1), umax = fmaxf(u0, u1);
-#pragma unroll
-          for (int msk = 4; msk < 32; msk <<= 1) {
-            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, msk));
-            umax = fmaxf(umax, __shfl_xor_sync(0xffffffffu, umax, msk));
-          }
-          const float m_new = fmaxf(m_run[nt][h], tmax);
-          const float mu_new = fmaxf(mu_run[nt][h], umax);
-          l_run[nt][h] = l_run[nt][h] * fast_exp2(m_run[nt][h] - m_new) + fast_exp2(s0 - m_new) +
-                         fast_exp2(s1 - m_new);
-          alpha_o[nt][h] = fast_exp2(mu_run[nt][h] - mu_new);
-          rescale |= mu_new != mu_run[nt][h];
-          m_run[nt][h] = m_new;
-          mu_run[nt][h] = mu_new;
-          w4[h] = fast_exp2(u0 - mu_new);
-          w4[2 + h] = fast_exp2(u1 - mu_new);
-        }
-        pw[nt][0] = movmatrix_trans(pack_f16x2(w4[0], w4[1]));
-        pw[nt][1] = movmatrix_trans(pack_f16x2(w4[2], w4[3]));
+  for (;;) {
+    if (threadIdx.x == 0) s_misc[0] = atomicAdd(&ws.hdr[1], 1);
+    __syncthreads();
+    const int u = s_misc[0];
+    if (u >= n_units || s_misc[1]) break;
+    const uint32_t unit = ws.units[u];
+    const int b = (int)(unit & 0xffffu), split = (int)((unit >> 16) & 0xffu), g = (int)(unit >> 24);
+    const int L = clamp_len(seq_lens[b], max_blocks);
+    const int pps = ws.seq_info[b].x;
+    const int P = (L + kPage - 1) / kPage;
+    const int p_begin = split * pps;
+    const int p_end = min(p_begin + pps, P);
+
+    // ---- per-warp page schedule ---------------------------------------------
+    const int n_pages = p_end - p_begin;
+    const int n_my = n_pages > warp ? (n_pages - warp + NWARPS - 1) / NWARPS : 0;
+    const int32_t* bt_row = block_table + (int64_t)b * max_blocks + p_begin + warp;
+    int pid_chunk = -1, pid_reg = -1;
+
+    auto issue = [&](int j, int stg) {
+      const int chunk = j >> 5;
+      if (chunk != pid_chunk) {
+        const int jj = chunk * 32 + lane;
+        pid_reg = jj < n_my ? bt_row[(int64_t)jj * NWARPS] : -1;
+        pid_chunk = chunk;
       }
-      if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int mt = 0; mt < 16; ++mt) {
-            o[nt][mt][0] *= alpha_o[nt][0];
-            o[nt][mt][1] *= alpha_o[nt][1];
-            o[nt][mt][2] *= alpha_o[nt][0];
-            o[nt][mt][3] *= alpha_o[nt][1];
-          }
-      }
-      // -- PV on the tensor cores
-      const uint32_t voff = kVCodeOff + 16 * gq;
-      const uint4 va = lds128(sb + ta * kSlotBytes + voff);
-      const uint4 vb = lds128(sb + tb * kSlotBytes + voff);
-      const uint4 vc = lds128(sb + tcc * kSlotBytes + voff);
-      const uint4 vd = lds128(sb + td * kSlotBytes + voff);
-      const uint32_t vaw[4] = {va.x, va.y, va.z, va.w}, vbw[4] = {vb.x, vb.y, vb.z, vb.w};
-      const uint32_t vcw[4] = {vc.x, vc.y, vc.z, vc.w}, vdw[4] = {vd.x, vd.y, vd.z, vd.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        // pair the same head dim of two tokens in one byte: (token t+1 << 4) | token t
-        const uint32_t lo01 = (vaw[q] & 0x0F0F0F0Fu) | ((vbw[q] << 4) & 0xF0F0F0F0u);
-        const uint32_t hi01 = ((vaw[q] >> 4) & 0x0F0F0F0Fu) | (vbw[q] & 0xF0F0F0F0u);
-        const uint32_t lo89 = (vcw[q] & 0x0F0F0F0Fu) | ((vdw[q] << 4) & 0xF0F0F0F0u);
-        const uint32_t hi89 = ((vcw[q] >> 4) & 0x0F0F0F0Fu) | (vdw[q] & 0xF0F0F0F0u);
-        uint32_t A0[4], A1[4], A2[4], A3[4];
-        f16x2x4_from_e2m1_word(lo01, A0);
-        f16x2x4_from_e2m1_word(hi01, A1);
-        f16x2x4_from_e2m1_word(lo89, A2);
-        f16x2x4_from_e2m1_word(hi89, A3);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const uint32_t a0 = hmul2(A0[e], rv01), a1 = hmul2(A1[e], rv01);
-          const uint32_t a2 = hmul2(A2[e], rv89), a3 = hmul2(A3[e], rv89);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-            mma_f16_16816(o[nt][4 * q + e], a0, a1, a2, a3, pw[nt][0], pw[nt][1]);
+      const int pid = __shfl_sync(0xffffffffu, pid_reg, j & 31);
+      const uint32_t bar = bar_base + 8 * stg;
+      const bool ok = (unsigned)pid < (unsigned)num_blocks;
+      stage_ok = ok ? (stage_ok | (1u << stg)) : (stage_ok & ~(1u << stg));
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        if (ok) {
+          mbar_arrive_expect_tx(bar, kTileBytes);
+        } else {
+          atomicOr(err, kErrBadPage);
+          mbar_arrive(bar);
         }
+      }
+      __syncwarp();
+      if (ok && lane < kPage) {
+        const uint8_t* src = kv + (((int64_t)pid * kPage + lane) * Hk + g) * (int64_t)kSlotBytes;
+        bulk_g2s(stage_base + stg * kTileBytes + lane * kSlotBytes, src, kSlotBytes, bar);
+      }
+    };
+
+    // this unit's first tile lands in stage tiles_done % NSTAGE, phase parity
+    // (tiles_done / NSTAGE) & 1; later tiles advance both incrementally
+    const int stg0 = (int)(tiles_done % NSTAGE);
+    const uint32_t ph0 = (tiles_done / NSTAGE) & 1u;
+    for (int j = 0; j < NSTAGE && j < n_my; ++j) issue(j, (stg0 + j) % NSTAGE);
+
+    // ---- query prologue: q' = f16(e4m3(fp32(q) H)) in operand order -----------
+    // Row r, k-step i, position kp holds head dim 64c + 4i + e with
+    // kp = 2c + (e & 1) + 8 (e >> 1).
+    for (int r = warp; r < Lay::kRows; r += NWARPS) {
+      uint8_t* row = reinterpret_cast<uint8_t*>(qs) + r * Lay::kQRowBytes;
+      uint32_t pk[4] = {0u, 0u, 0u, 0u};
+      if (r < QG) {
+        const uint16_t* qp = query + (int64_t)b * q_ss + (int64_t)(g * QG + r) * q_sh + lane * 8;
+        const uint4 raw = *reinterpret_cast<const uint4*>(qp);
+        float x[8];
+        const uint32_t uu[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          x[2 * i] = bf16_bits_to_f32(uu[i] & 0xffffu);
+          x[2 * i + 1] = bf16_bits_to_f32(uu[i] >> 16);
+        }
+#pragma unroll
+        for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if ((i & h) == 0) {
+              const float a = x[i], cc = x[i + h];
+              x[i] = a + cc;
+              x[i + h] = a - cc;
+            }
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) {
+          const bool upper = (lane & m) != 0;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float other = __shfl_xor_sync(0xffffffffu, x[i], m);
+            x[i] = upper ? (other - x[i]) : (x[i] + other);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) pk[i] = e4m3_roundtrip_f16x2(x[2 * i] * 0.0625f, x[2 * i + 1] * 0.0625f);
+      }
+      // lane holds head dims 8*lane .. 8*lane+7: c' = lane / 8, k-steps 2(lane % 8) + {0, 1}
+      const int cq = lane >> 3, i0 = 2 * (lane & 7);
+#pragma unroll
+      for (int ii = 0; ii < 2; ++ii) {
+        uint8_t* kstep = row + (i0 + ii) * 32;
+        *reinterpret_cast<uint32_t*>(kstep + 4 * cq) = pk[2 * ii];          // kp 2c', 2c'+1
+        *reinterpret_cast<uint32_t*>(kstep + 16 + 4 * cq) = pk[2 * ii + 1]; // kp 2c'+8, 2c'+9
       }
     }
-    __syncwarp();
-    if (j + NSTAGE < n_my) issue(j + NSTAGE);
-  }
-  if (timed_out) {
-    if (lane == 0) atomicOr(err, kErrTimeout);
-    // wait (bounded) for this warp's copies still in flight before leaving
-    for (int jj = j; jj < n_my && jj < j + NSTAGE; ++jj)
-      (void)mbar_wait(bar_base + 8 * (jj % NSTAGE), (uint32_t)((jj / NSTAGE) & 1));
+    __syncthreads();
+
+    // ldmatrix row addresses: lane -> matrix lane/8 (k-step +(lane>>4), half (lane>>3)&1), row lane%8
+    const uint32_t q_lds = smem_u32(qs) + (lane & 7) * Lay::kQRowBytes + (lane >> 4) * 32 + ((lane >> 3) & 1) * 16;
+
+    // ---- main loop over this warp's pages -------------------------------------
+    float o[NT][16][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int mt = 0; mt < 16; ++mt) o[nt][mt][0] = o[nt][mt][1] = o[nt][mt][2] = o[nt][mt][3] = 0.f;
+    float m_run[NT][2], mu_run[NT][2], l_run[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -387,90 +390,279 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
         mu_run[nt][h] = -INFINITY;
         l_run[nt][h] = 0.f;
       }
-  }
-  // full row sums over the 8 lanes that share c
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-      for (int msk = 4; msk < 32; msk <<= 1)
-        l_run[nt][h] += __shfl_xor_sync(0xffffffffu, l_run[nt][h], msk);
 
-  // ---- merge the warps' states: partial (o, lse) of this split -------------
-  __syncthreads();  // every warp is done with its stage buffers
-  float* osm = reinterpret_cast<float*>(smem);
-  float* stats = reinterpret_cast<float*>(smem + Lay::kStatsOff);
-  float* rowinfo = reinterpret_cast<float*>(smem + Lay::kRowInfoOff);
-  float* my_o = osm + warp * Lay::kRows * Lay::kORowStride;
+    bool timed_out = false;
+    int j = 0;
+    int stg = stg0;
+    uint32_t phase = ph0;
+    for (; j < n_my; ++j) {
+      if (!mbar_wait(bar_base + 8 * stg, phase)) {
+        timed_out = true;
+        break;
+      }
+      const int page = p_begin + warp + j * NWARPS;
+      const int nvalid = ((stage_ok >> stg) & 1u) ? min(kPage, L - page * kPage) : 0;
+      if (nvalid > 0) {
+        const uint32_t sb = stage_base + stg * kTileBytes;
+        // -- tile metadata, one (token, K or V) scale row per lane: the token's
+        //    largest block byte E, the 8 relative scales 2^(byte - E) as f16
+        //    and one fp32 factor (K: scale*log2e*2^(E-127); V: E-127)
+        {
+          const int mtok = lane & 15, kind = lane >> 4;
+          const uint2 sc = lds64(sb + mtok * kSlotBytes + kKScaleOff + 8 * kind);
+          const uint32_t E = max_byte8(sc.x, sc.y);
+          uint32_t p[4];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int r0 = nt * 8 + 2 * c;
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t w = k < 2 ? sc.x : sc.y;
+            const uint32_t b0 = (w >> (16 * (k & 1))) & 0xffu, b1 = (w >> (16 * (k & 1) + 8)) & 0xffu;
+            p[k] = (lds32(lut_base + 4 * (E - b0)) & 0xffffu) | (lds32(lut_base + 4 * (E - b1)) & 0xffff0000u);
+          }
+          sts128(meta_rel + (kind * kPage + mtok) * 16, make_uint4(p[0], p[1], p[2], p[3]));
+          const float f = kind == 0 ? scale_log2e * ue8m0_to_f32(E) : (float)((int)E - 127);
+          sts32(meta_f + (kind * kPage + mtok) * 4, __float_as_uint(f));
+        }
+        __syncwarp();
+        // K relative scales of tokens gq, gq+8 for blocks 2c, 2c+1 as f16x2 (both halves)
+        const uint32_t kr0 = lds32(meta_rel + gq * 16 + 4 * c);
+        const uint32_t kr1 = lds32(meta_rel + (gq + 8) * 16 + 4 * c);
+        const uint32_t rk0[2] = {__byte_perm(kr0, 0, 0x1010), __byte_perm(kr0, 0, 0x3232)};
+        const uint32_t rk1[2] = {__byte_perm(kr1, 0, 0x1010), __byte_perm(kr1, 0, 0x3232)};
+        // -- QK on the tensor cores, NCH independent accumulation chains
+        const uint4 ka0 = lds128(sb + gq * kSlotBytes + 32 * c);
+        const uint4 ka1 = lds128(sb + gq * kSlotBytes + 32 * c + 16);
+        const uint4 kb0 = lds128(sb + (gq + 8) * kSlotBytes + 32 * c);
+        const uint4 kb1 = lds128(sb + (gq + 8) * kSlotBytes + 32 * c + 16);
+        const uint32_t kaw[8] = {ka0.x, ka0.y, ka0.z, ka0.w, ka1.x, ka1.y, ka1.z, ka1.w};
+        const uint32_t kbw[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
+        float sacc[NT][NCH][4];
 #pragma unroll
-    for (int mt = 0; mt < 16; ++mt) {
-      const int d = 32 * gq + 2 * mt;
-      *reinterpret_cast<float2*>(my_o + r0 * Lay::kORowStride + d) = make_float2(o[nt][mt][0], o[nt][mt][2]);
-      *reinterpret_cast<float2*>(my_o + (r0 + 1) * Lay::kORowStride + d) = make_float2(o[nt][mt][1], o[nt][mt][3]);
-    }
-    if (gq == 0) {
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float* st = stats + (warp * Lay::kRows + r0 + h) * 4;
-        st[0] = m_run[nt][h];
-        st[1] = mu_run[nt][h];
-        st[2] = l_run[nt][h];
+          for (int ch = 0; ch < NCH; ++ch) sacc[nt][ch][0] = sacc[nt][ch][1] = sacc[nt][ch][2] = sacc[nt][ch][3] = 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          uint32_t fa[4], fb[4];
+          f16x2x4_from_e2m1_word(kaw[q], fa);
+          f16x2x4_from_e2m1_word(kbw[q], fb);
+          const uint32_t ra = rk0[q >> 2], rb = rk1[q >> 2];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            fa[e] = hmul2(fa[e], ra);
+            fb[e] = hmul2(fb[e], rb);
+          }
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            uint32_t b0, b1, b2, b3;   // k-step 2q: (b0, b1), k-step 2q+1: (b2, b3)
+            ldmatrix_x4(q_lds + nt * 8 * Lay::kQRowBytes + q * 64, b0, b1, b2, b3);
+            mma_f16_16816(sacc[nt][(2 * q) % NCH], fa[0], fb[0], fa[1], fb[1], b0, b1);
+            mma_f16_16816(sacc[nt][(2 * q + 1) % NCH], fa[2], fb[2], fa[3], fb[3], b2, b3);
+          }
+        }
+        // -- V relative scales of tokens 2c, 2c+1, 2c+8, 2c+9 for block gq, and the
+        //    K / V factors of tokens gq, gq+8
+        const uint32_t vrel = meta_rel + kPage * 16 + 2 * gq;
+        const uint32_t rv01 = __byte_perm(lds16(vrel + ta * 16), lds16(vrel + tb * 16), 0x5410);
+        const uint32_t rv89 = __byte_perm(lds16(vrel + tcc * 16), lds16(vrel + td * 16), 0x5410);
+        const float fk0 = __uint_as_float(lds32(meta_f + gq * 4));
+        const float fk1 = __uint_as_float(lds32(meta_f + (gq + 8) * 4));
+        const float evf0 = __uint_as_float(lds32(meta_f + (kPage + gq) * 4));
+        const float evf1 = __uint_as_float(lds32(meta_f + (kPage + gq + 8) * 4));
+
+        // -- scores and online softmax
+        const bool v0 = gq < nvalid, v1 = gq + 8 < nvalid;
+        uint32_t pw[NT][2];
+        bool rescale = false;
+        float alpha_o[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          float sres[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            float acc = sacc[nt][0][k];
+#pragma unroll
+            for (int ch = 1; ch < NCH; ++ch) acc += sacc[nt][ch][k];
+            sres[k] = acc;
+          }
+          float w4[4];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float s0 = v0 ? sres[h] * fk0 : -INFINITY;
+            const float s1 = v1 ? sres[2 + h] * fk1 : -INFINITY;
+            const float u0 = s0 + evf0;
+            const float u1 = s1 + evf1;
+            float tmax = fmaxf(s0, s1), umax = fmaxf(u0, u1);
+#pragma unroll
+            for (int msk = 4; msk < 32; msk <<= 1) {
+              tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, msk));
+              umax = fmaxf(umax, __shfl_xor_sync(0xffffffffu, umax, msk));
+            }
+            const float m_new = fmaxf(m_run[nt][h], tmax);
+            const float mu_new = fmaxf(mu_run[nt][h], umax);
+            l_run[nt][h] = l_run[nt][h] * fast_exp2(m_run[nt][h] - m_new) + fast_exp2(s0 - m_new) +
+                           fast_exp2(s1 - m_new);
+            alpha_o[nt][h] = fast_exp2(mu_run[nt][h] - mu_new);
+            rescale |= mu_new != mu_run[nt][h];
+            m_run[nt][h] = m_new;
+            mu_run[nt][h] = mu_new;
+            w4[h] = fast_exp2(u0 - mu_new);
+            w4[2 + h] = fast_exp2(u1 - mu_new);
+          }
+          pw[nt][0] = movmatrix_trans(pack_f16x2(w4[0], w4[1]));
+          pw[nt][1] = movmatrix_trans(pack_f16x2(w4[2], w4[3]));
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int mt = 0; mt < 16; ++mt) {
+              o[nt][mt][0] *= alpha_o[nt][0];
+              o[nt][mt][1] *= alpha_o[nt][1];
+              o[nt][mt][2] *= alpha_o[nt][0];
+              o[nt][mt][3] *= alpha_o[nt][1];
+            }
+        }
+        // -- PV on the tensor cores
+        const uint32_t voff = kVCodeOff + 16 * gq;
+        const uint4 va = lds128(sb + ta * kSlotBytes + voff);
+        const uint4 vb = lds128(sb + tb * kSlotBytes + voff);
+        const uint4 vc = lds128(sb + tcc * kSlotBytes + voff);
+        const uint4 vd = lds128(sb + td * kSlotBytes + voff);
+        const uint32_t vaw[4] = {va.x, va.y, va.z, va.w}, vbw[4] = {vb.x, vb.y, vb.z, vb.w};
+        const uint32_t vcw[4] = {vc.x, vc.y, vc.z, vc.w}, vdw[4] = {vd.x, vd.y, vd.z, vd.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          // pair the same head dim of two tokens in one byte: (token t+1 << 4) | token t
+          const uint32_t lo01 = (vaw[q] & 0x0F0F0F0Fu) | ((vbw[q] << 4) & 0xF0F0F0F0u);
+          const uint32_t hi01 = ((vaw[q] >> 4) & 0x0F0F0F0Fu) | (vbw[q] & 0xF0F0F0F0u);
+          const uint32_t lo89 = (vcw[q] & 0x0F0F0F0Fu) | ((vdw[q] << 4) & 0xF0F0F0F0u);
+          const uint32_t hi89 = ((vcw[q] >> 4) & 0x0F0F0F0Fu) | (vdw[q] & 0xF0F0F0F0u);
+          uint32_t A0[4], A1[4], A2[4], A3[4];
+          f16x2x4_from_e2m1_word(lo01, A0);
+          f16x2x4_from_e2m1_word(hi01, A1);
+          f16x2x4_from_e2m1_word(lo89, A2);
+          f16x2x4_from_e2m1_word(hi89, A3);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t a0 = hmul2(A0[e], rv01), a1 = hmul2(A1[e], rv01);
+            const uint32_t a2 = hmul2(A2[e], rv89), a3 = hmul2(A3[e], rv89);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              mma_f16_16816(o[nt][4 * q + e], a0, a1, a2, a3, pw[nt][0], pw[nt][1]);
+          }
+        }
+      }
+      __syncwarp();
+      if (j + NSTAGE < n_my) issue(j + NSTAGE, stg);   // same stage, next phase
+      if (++stg == NSTAGE) {
+        stg = 0;
+        phase ^= 1u;
       }
     }
-  }
-  __syncthreads();
-  if (threadIdx.x < QG) {
-    const int r = threadIdx.x;
-    float M = -INFINITY;
-    for (int w = 0; w < NWARPS; ++w) M = fmaxf(M, stats[(w * Lay::kRows + r) * 4]);
-    float Ls = 0.f;
-    for (int w = 0; w < NWARPS; ++w) {
-      const float* st = stats + (w * Lay::kRows + r) * 4;
-      if (st[2] > 0.f) Ls += st[2] * fast_exp2(st[0] - M);
-    }
-    float* ri = rowinfo + r * (NWARPS + 2);
-    for (int w = 0; w < NWARPS; ++w) {
-      const float* st = stats + (w * Lay::kRows + r) * 4;
-      ri[w] = (Ls > 0.f && st[2] > 0.f) ? fast_exp2(st[1] - M) / Ls : 0.f;
-    }
-    ri[NWARPS] = Ls > 0.f ? M + fast_log2(Ls) : -INFINITY;
-    part_lse[((int64_t)(b * Hq + g * QG + r)) * S + split] = ri[NWARPS];
-  }
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < QG * (kHeadDim / 4); idx += NWARPS * 32) {
-    const int r = idx / (kHeadDim / 4), d4 = (idx % (kHeadDim / 4)) * 4;
-    const float* ri = rowinfo + r * (NWARPS + 2);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (timed_out) {
+      if (lane == 0) atomicOr(err, kErrTimeout);
+      // wait (bounded) for this warp's copies still in flight, then stop the CTA
+      for (int jj = j; jj < n_my && jj < j + NSTAGE; ++jj) {
+        (void)mbar_wait(bar_base + 8 * stg, phase);
+        if (++stg == NSTAGE) {
+          stg = 0;
+          phase ^= 1u;
+        }
+      }
+      s_misc[1] = 1;
 #pragma unroll
-    for (int w = 0; w < NWARPS; ++w) {
-      const float f = ri[w];
-      const float4 v = *reinterpret_cast<const float4*>(osm + (w * Lay::kRows + r) * Lay::kORowStride + d4);
-      acc.x += v.x * f;
-      acc.y += v.y * f;
-      acc.z += v.z * f;
-      acc.w += v.w * f;
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          m_run[nt][h] = -INFINITY;
+          mu_run[nt][h] = -INFINITY;
+          l_run[nt][h] = 0.f;
+        }
     }
-    *reinterpret_cast<float4*>(part_o + (((int64_t)(b * Hq + g * QG + r)) * S + split) * kHeadDim + d4) = acc;
+    tiles_done += (uint32_t)n_my;
+    // full row sums over the 8 lanes that share c
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int msk = 4; msk < 32; msk <<= 1)
+          l_run[nt][h] += __shfl_xor_sync(0xffffffffu, l_run[nt][h], msk);
+
+    // ---- merge the warps' states: partial (o, lse) of this split ---------------
+    __syncthreads();  // every warp is done with its stage buffers
+    float* osm = reinterpret_cast<float*>(smem);
+    float* stats = reinterpret_cast<float*>(smem + Lay::kStatsOff);
+    float* rowinfo = reinterpret_cast<float*>(smem + Lay::kRowInfoOff);
+    float* my_o = osm + warp * Lay::kRows * Lay::kORowStride;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int r0 = nt * 8 + 2 * c;
+#pragma unroll
+      for (int mt = 0; mt < 16; ++mt) {
+        const int d = 32 * gq + 2 * mt;
+        *reinterpret_cast<float2*>(my_o + r0 * Lay::kORowStride + d) = make_float2(o[nt][mt][0], o[nt][mt][2]);
+        *reinterpret_cast<float2*>(my_o + (r0 + 1) * Lay::kORowStride + d) = make_float2(o[nt][mt][1], o[nt][mt][3]);
+      }
+      if (gq == 0) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float* st = stats + (warp * Lay::kRows + r0 + h) * 4;
+          st[0] = m_run[nt][h];
+          st[1] = mu_run[nt][h];
+          st[2] = l_run[nt][h];
+        }
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x < QG) {
+      const int r = threadIdx.x;
+      float M = -INFINITY;
+      for (int w = 0; w < NWARPS; ++w) M = fmaxf(M, stats[(w * Lay::kRows + r) * 4]);
+      float Ls = 0.f;
+      for (int w = 0; w < NWARPS; ++w) {
+        const float* st = stats + (w * Lay::kRows + r) * 4;
+        if (st[2] > 0.f) Ls += st[2] * fast_exp2(st[0] - M);
+      }
+      float* ri = rowinfo + r * (NWARPS + 2);
+      for (int w = 0; w < NWARPS; ++w) {
+        const float* st = stats + (w * Lay::kRows + r) * 4;
+        ri[w] = (Ls > 0.f && st[2] > 0.f) ? fast_exp2(st[1] - M) / Ls : 0.f;
+      }
+      ri[NWARPS] = Ls > 0.f ? M + fast_log2(Ls) : -INFINITY;
+      ws.part_lse[((int64_t)(b * Hq + g * QG + r)) * S + split] = ri[NWARPS];
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < QG * (kHeadDim / 4); idx += NWARPS * 32) {
+      const int r = idx / (kHeadDim / 4), d4 = (idx % (kHeadDim / 4)) * 4;
+      const float* ri = rowinfo + r * (NWARPS + 2);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int w = 0; w < NWARPS; ++w) {
+        const float f = ri[w];
+        const float4 v = *reinterpret_cast<const float4*>(osm + (w * Lay::kRows + r) * Lay::kORowStride + d4);
+        acc.x += v.x * f;
+        acc.y += v.y * f;
+        acc.z += v.z * f;
+        acc.w += v.w * f;
+      }
+      *reinterpret_cast<float4*>(ws.part_o + (((int64_t)(b * Hq + g * QG + r)) * S + split) * kHeadDim + d4) = acc;
+    }
+    __syncthreads();  // merge buffers (stage buffers) and Q' are free again
   }
 }
 
+// ---------------------------------------------------------------------------
 // Stage 2: merge the active splits of each (sequence, query head).
+// ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(128)
-decode_stage2(const float* __restrict__ part_o, const float* __restrict__ part_lse,
-              const int32_t* __restrict__ seq_lens, int B, int Hq, int S, int max_blocks,
-              uint16_t* __restrict__ out) {
+decode_stage2(Workspace ws, int B, int Hq, int S, uint16_t* __restrict__ out) {
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
   if (row >= B * Hq) return;
   const int b = row / Hq;
-  const int L = clamp_len(seq_lens[b], max_blocks);
-  const SplitPlan plan = split_plan(L, S);
-  const int n = plan.n_active;
-  const float* lse = part_lse + (int64_t)row * S;
+  const int n = ws.seq_info[b].y;
+  const float* lse = ws.part_lse + (int64_t)row * S;
   float mx = -INFINITY;
   for (int s = lane; s < n; s += 32) mx = fmaxf(mx, lse[s]);
 #pragma unroll
@@ -478,7 +670,7 @@ decode_stage2(const float* __restrict__ part_o, const float* __restrict__ part_l
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   float den = 0.f;
   if (n > 0 && mx > -INFINITY) {
-    const float* po = part_o + (int64_t)row * S * kHeadDim + lane * 8;
+    const float* po = ws.part_o + (int64_t)row * S * kHeadDim + lane * 8;
     for (int s0 = 0; s0 < n; s0 += 32) {
       const float wl = (s0 + lane < n) ? fast_exp2(lse[s0 + lane] - mx) : 0.f;
       const int cnt = min(32, n - s0);
@@ -503,6 +695,9 @@ decode_stage2(const float* __restrict__ part_o, const float* __restrict__ part_l
   *reinterpret_cast<uint4*>(out + (int64_t)row * kHeadDim + lane * 8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
 }
 
+// ---------------------------------------------------------------------------
+// Host side.
+// ---------------------------------------------------------------------------
 // Record a caller's timing event.  Under stream capture a plain record only
 // becomes a dependency edge, so it is captured as an external event node.
 static cudaError_t record_timing_event(cudaEvent_t ev, cudaStream_t stream) {
@@ -514,52 +709,70 @@ static cudaError_t record_timing_event(cudaEvent_t ev, cudaStream_t stream) {
              : cudaEventRecord(ev, stream);
 }
 
+// Per device and instantiation: set the shared-memory opt-in once and size the
+// persistent grid from the occupancy the kernel actually gets.
+template <int NT>
+static cudaError_t stage1_grid(int* grid) {
+  constexpr int NWARPS = 4, NSTAGE = kStage1Stages;
+  using Lay = Stage1Layout<NT, NWARPS, NSTAGE>;
+  static int grid_of_device[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && grid_of_device[dev] > 0) {
+    *grid = grid_of_device[dev];
+    return cudaSuccess;
+  }
+  auto kern = decode_stage1<NT, NWARPS, NSTAGE>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
+  if (e != cudaSuccess) return e;
+  int sms = 0, per_sm = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NWARPS * 32, Lay::kBytes);
+  if (e != cudaSuccess) return e;
+  *grid = sms * (per_sm > 0 ? per_sm : 1);
+  if (dev >= 0 && dev < 64) grid_of_device[dev] = *grid;
+  return cudaSuccess;
+}
+
 template <int NT>
 static cudaError_t launch_stage1_t(const uint16_t* query, int64_t q_ss, int64_t q_sh,
                                    const uint8_t* kv, const int32_t* bt, const int32_t* sl,
                                    float scale, int B, int Hq, int Hk, int num_blocks,
-                                   int max_blocks, int S, float* part_o, float* part_lse,
-                                   unsigned* err, cudaStream_t stream) {
-  constexpr int NWARPS = 4, NSTAGE = 3;
+                                   int max_blocks, int S, const Workspace& ws, unsigned* err,
+                                   cudaStream_t stream, cudaEvent_t ev_before, cudaEvent_t ev_after) {
+  constexpr int NWARPS = 4, NSTAGE = kStage1Stages;
   using Lay = Stage1Layout<NT, NWARPS, NSTAGE>;
-  auto kern = decode_stage1<NT, NWARPS, NSTAGE>;
-  static int configured_mask = 0;  // one bit per device (first 31 devices)
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 31 || !(configured_mask & (1 << dev))) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
-    if (e != cudaSuccess) return e;
-    if (dev < 31) configured_mask |= 1 << dev;
-  }
-  dim3 grid(S, Hk, B);
-  kern<<<grid, NWARPS * 32, Lay::kBytes, stream>>>(query, q_ss, q_sh, kv, bt, sl, scale * kLog2e,
-                                                   Hq, Hk, Hq / Hk, num_blocks, max_blocks, S,
-                                                   part_o, part_lse, err);
-  return cudaGetLastError();
+  int grid = 0;
+  cudaError_t e = stage1_grid<NT>(&grid);
+  if (e != cudaSuccess) return e;
+  decode_plan<<<1, kPlanThreads, 0, stream>>>(sl, B, Hk, S, max_blocks, grid * kUnitsPerCta, ws);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (ev_before && (e = record_timing_event(ev_before, stream)) != cudaSuccess) return e;
+  decode_stage1<NT, NWARPS, NSTAGE><<<grid, NWARPS * 32, Lay::kBytes, stream>>>(
+      query, q_ss, q_sh, kv, bt, sl, scale * kLog2e, Hq, Hk, Hq / Hk, num_blocks, max_blocks, S,
+      ws, err);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (ev_after && (e = record_timing_event(ev_after, stream)) != cudaSuccess) return e;
+  return cudaSuccess;
 }
+
+size_t decode_workspace_bytes(int B, int Hq, int S) { return workspace_bytes(B, Hq, S); }
 
 cudaError_t launch_decode(const uint16_t* query, int64_t q_ss, int64_t q_sh, const uint8_t* kv,
                           const int32_t* bt, const int32_t* sl, float scale, int B, int Hq,
                           int Hk, int num_blocks, int max_blocks, int S, void* workspace,
                           uint16_t* out, unsigned* err, cudaStream_t stream,
                           cudaEvent_t ev_before_stage1, cudaEvent_t ev_after_stage1) {
-  float* part_o = static_cast<float*>(workspace);
-  float* part_lse = part_o + (size_t)B * Hq * S * kHeadDim;
+  const Workspace ws = workspace_layout(workspace, B, Hq, S);
   const int QG = Hq / Hk;
-  if (ev_before_stage1) {
-    cudaError_t er = record_timing_event(ev_before_stage1, stream);
-    if (er != cudaSuccess) return er;
-  }
   cudaError_t e = (QG == 16)
-      ? launch_stage1_t<2>(query, q_ss, q_sh, kv, bt, sl, scale, B, Hq, Hk, num_blocks, max_blocks, S, part_o, part_lse, err, stream)
-      : launch_stage1_t<1>(query, q_ss, q_sh, kv, bt, sl, scale, B, Hq, Hk, num_blocks, max_blocks, S, part_o, part_lse, err, stream);
+      ? launch_stage1_t<2>(query, q_ss, q_sh, kv, bt, sl, scale, B, Hq, Hk, num_blocks, max_blocks, S, ws, err, stream, ev_before_stage1, ev_after_stage1)
+      : launch_stage1_t<1>(query, q_ss, q_sh, kv, bt, sl, scale, B, Hq, Hk, num_blocks, max_blocks, S, ws, err, stream, ev_before_stage1, ev_after_stage1);
   if (e != cudaSuccess) return e;
-  if (ev_after_stage1) {
-    e = record_timing_event(ev_after_stage1, stream);
-    if (e != cudaSuccess) return e;
-  }
   const int rows = B * Hq;
-  decode_stage2<<<(rows + 3) / 4, 128, 0, stream>>>(part_o, part_lse, sl, B, Hq, S, max_blocks, out);
+  decode_stage2<<<(rows + 3) / 4, 128, 0, stream>>>(ws, B, Hq, S, out);
   return cudaGetLastError();
 }
 

@@ -14,9 +14,12 @@ constexpr int kKScaleOff = 256;
 constexpr int kVScaleOff = 264;
 constexpr int kVCodeOff = 128;
 
-// Iteration cap of every spin-wait (about a second of polling): a wait that
-// runs out sets UQ_DEVERR_TIMEOUT and the kernel returns instead of hanging.
-constexpr uint32_t kWaitSpinLimit = 1u << 24;
+// Bounded waits: each try_wait may suspend the thread for up to
+// kWaitSuspendNs (it returns as soon as the phase completes), and a wait
+// gives up after kWaitSpinLimit tries (about two seconds), sets
+// UQ_DEVERR_TIMEOUT and lets the kernel return instead of hanging.
+constexpr uint32_t kWaitSuspendNs = 1u << 16;
+constexpr uint32_t kWaitSpinLimit = 1u << 15;
 
 constexpr unsigned kErrBadPage = 1u;
 constexpr unsigned kErrBadSlot = 2u;
@@ -155,9 +158,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+        : "=r"(done) : "r"(bar), "r"(parity), "r"(kWaitSuspendNs) : "memory");
     if (done) return true;
   }
   return false;
@@ -185,6 +188,27 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
   return v;
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" :: "r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};"
+               :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
 __device__ __forceinline__ uint2 lds64(uint32_t addr) {

@@ -22,7 +22,7 @@ uq_status set_error(uq_status code, const char* msg);
 namespace {
 
 // Upper bound of uq_decode_workspace_bytes(B, Hq, 256, S) that the static
-// scratch can serve: 32 MiB, i.e. B * Hq * S <= 32640.
+// scratch can serve: 32 MiB, roughly B * Hq * S <= 32480.
 constexpr size_t kStaticScratchBytes = size_t(32) << 20;
 constexpr int kMaxDevices = 64;
 
@@ -44,7 +44,7 @@ extern "C" uq_status uq_decode_static_scratch(
   if (B > 0 && need > kStaticScratchBytes)
     return uq::set_error(UQ_ERR_WORKSPACE_TOO_SMALL,
                          "uq_decode_static_scratch: this batch needs more scratch than the "
-                         "library's fixed 32 MiB (B * Hq * max_num_kv_splits must be <= 32640); "
+                         "library's fixed 32 MiB (roughly B * Hq * max_num_kv_splits <= 32480); "
                          "use uq_decode with a caller-provided workspace");
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

@@ -76,13 +76,15 @@ size_t uq_slot_bytes(int head_dim);
 
 /*
  * Workspace bytes uq_decode needs for a batch of up to B sequences with Hq
- * query heads and max_num_kv_splits splits: the per-split partial outputs
- * (fp32, D values) and their log-sum-exp (fp32) for every (sequence, query
- * head, split), i.e. B * Hq * S * (D + 1) * 4, rounded up to 256 bytes.  It
+ * query heads and max_num_kv_splits splits: per (sequence, query head,
+ * split) the split's partial output (256 fp32), its log-sum-exp (fp32) and
+ * one 4-byte work-list entry, plus 12 bytes per sequence and a 64-byte
+ * header, i.e. B * Hq * S * 1032 + 12 * B + 64, rounded up to 256 bytes.  It
  * depends only on its arguments, so a caller can size the workspace once for
  * its largest batch before capturing a CUDA graph (the reference pre-grows
  * its pool before capture for the same reason, _ensure_on_device and
- * _SegmBufPool).  Returns 0 for invalid arguments.
+ * _SegmBufPool).  Returns 0 for invalid arguments (B < 1, Hq < 1, head_dim
+ * != 256, S outside [1, 256]).
  */
 size_t uq_decode_workspace_bytes(int B, int Hq, int head_dim, int max_num_kv_splits);
 
@@ -154,9 +156,12 @@ uq_status uq_store_rotated_f32(const float *key_rot, const float *value,
  * E4M3 "haircut", round to nearest even, saturating); s_t = scale * q'.k_t
  * over the L tokens of the sequence, k_t the dequantised rotated K;
  * out = softmax(s) . V (dequantised), rounded to bf16.  A sequence with
- * L == 0 gets out = 0.  Tokens are divided into up to S splits of whole
- * pages; each split's partial output and log-sum-exp are merged by a second
- * kernel on the same stream.
+ * L == 0 gets out = 0.  Supported Hk <= 256, B <= 65535.  Three kernels run
+ * on the stream: a one-CTA plan that divides every sequence into up to S
+ * splits of whole pages (the split size is chosen on the device from the
+ * batch's total length, so the work list has a few units per resident CTA)
+ * and orders the units longest first; the split-KV kernel (persistent CTAs
+ * taking units from that list); and the merge of each row's splits.
  */
 uq_status uq_decode(const void *query, const void *kv_cache,
                     const int32_t *block_table, const int32_t *seq_lens,
@@ -179,8 +184,8 @@ uq_status uq_decode(const void *query, const void *kv_cache,
  *
  * Arguments are those of uq_decode without workspace and workspace_bytes.
  * A batch whose uq_decode_workspace_bytes(B, Hq, 256, max_num_kv_splits)
- * exceeds 32 MiB (B * Hq * max_num_kv_splits > 32640) is rejected with
- * UQ_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.  The call allocates
+ * exceeds 32 MiB (roughly B * Hq * max_num_kv_splits > 32480) is rejected
+ * with UQ_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.  The call allocates
  * nothing.  The first call on a device looks up the array's device address;
  * make that first call before any stream capture.  All calls on a device
  * share the one array, and it keeps the previous call's partials (nothing in

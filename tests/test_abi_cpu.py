@@ -42,7 +42,7 @@ def test_sizes_and_version(lib):
     assert lib.uq_slot_bytes(256) == 272
     assert lib.uq_slot_bytes(128) == 0
     n = lib.uq_decode_workspace_bytes(64, 48, 256, 32)
-    assert n == ((64 * 48 * 32 * 257 * 4 + 255) // 256) * 256
+    assert n == ((64 * 48 * 32 * 1032 + 12 * 64 + 64 + 255) // 256) * 256
     assert lib.uq_decode_workspace_bytes(1, 8, 128, 4) == 0
     assert lib.uq_decode_workspace_bytes(1, 8, 256, 0) == 0
     assert lib.uq_decode_workspace_bytes(1, 8, 256, 257) == 0
@@ -82,6 +82,7 @@ def _decode(lib, **kw):
     (dict(nb=0), binding.UQ_ERR_INVALID_ARG),
     (dict(B=-1), binding.UQ_ERR_INVALID_ARG),
     (dict(B=70000), binding.UQ_ERR_INVALID_ARG),
+    (dict(Hq=512 * 8, Hk=512, qss=512 * 8 * 256), binding.UQ_ERR_UNSUPPORTED),   # Hk > 256
     (dict(ws_bytes=1000), binding.UQ_ERR_WORKSPACE_TOO_SMALL),
     (dict(scale=float("nan")), binding.UQ_ERR_INVALID_ARG),
 ])

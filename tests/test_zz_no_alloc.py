@@ -63,7 +63,7 @@ def test_static_scratch_matches_uq_decode_two_calls_in_a_row():
 
 
 def test_static_scratch_at_its_size_limit():
-    # B * Hq * S = 32 * 32 * 31 = 31744 <= 32640 fits the 32 MiB array
+    # B * Hq * S = 32 * 32 * 31 = 31744 rows fit the 32 MiB array
     wl = workloads.decode_workload("batch")
     cache = fill_cache_gpu(wl)
     q = workloads.query(wl, "cuda")
@@ -72,7 +72,7 @@ def test_static_scratch_at_its_size_limit():
 
 
 def test_static_scratch_rejects_oversize_batch():
-    wl = workloads.decode_workload("batch")              # 32 * 32 * 32 = 32768 > 32640
+    wl = workloads.decode_workload("batch")              # 32 * 32 * 32 = 32768 rows do not
     L = lib()
     cache = torch.zeros((1, 16, wl.Hk, 272), dtype=torch.uint8, device="cuda")
     q = torch.zeros((wl.B, wl.Hq, 256), dtype=torch.bfloat16, device="cuda")
