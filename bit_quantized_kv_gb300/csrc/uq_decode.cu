@@ -16,8 +16,10 @@
 // Stage 1 (persistent: resident CTAs only, 4 warps each).  Each CTA takes
 // units from the counter.  Inside a unit each warp takes every 4th page and
 // keeps its own online-softmax state; a page's 16 slots of one kv head
-// (16 x 272 B) arrive in shared memory by bulk async copies completing on a
-// per-stage mbarrier, NSTAGE pages ahead.  The unit's query group (6, 8 or 16
+// (16 x 272 B, strided by Hk * 272 B in the cache) arrive in shared memory as
+// one TMA tile copy (a 3-D tensor map over the cache: 68 words x Hk heads x
+// slots, box 68 x 1 x 16) completing on a per-stage mbarrier, NSTAGE pages
+// ahead.  One lane issues each copy with warp-uniform operands.  The unit's query group (6, 8 or 16
 // rows) is rotated (fp32 butterfly, x 1/16), rounded through E4M3 and kept
 // in shared memory as f16 in tensor-core operand order.  At the end of the
 // unit the four warps' states are merged into one split partial.
@@ -38,6 +40,9 @@
 //
 // Stage 2: one warp per (sequence, query head) merges the active splits with
 // the log-sum-exp rule and writes bf16.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "uq_device.cuh"
 
 namespace uq {
@@ -51,10 +56,10 @@ constexpr int kTileBytes = kPage * kSlotBytes;   // 4352 bytes per (page, kv hea
 #define UQ_UNITS_PER_CTA 4
 #endif
 #ifndef UQ_S1_NSTAGE
-#define UQ_S1_NSTAGE 3
+#define UQ_S1_NSTAGE 2
 #endif
 #ifndef UQ_S1_MIN_BLOCKS
-#define UQ_S1_MIN_BLOCKS 3
+#define UQ_S1_MIN_BLOCKS 4
 #endif
 constexpr int kMinPagesPerUnit = UQ_MIN_PAGES_PER_UNIT;  // floor of 128 tokens per split
 constexpr int kUnitsPerCta = UQ_UNITS_PER_CTA;           // work units per resident CTA
@@ -237,7 +242,7 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_
 template <int NT, int NWARPS, int NSTAGE>
 __global__ void __launch_bounds__(NWARPS * 32, NT == 1 ? UQ_S1_MIN_BLOCKS : 2)
 decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
-              const uint8_t* __restrict__ kv, const int32_t* __restrict__ block_table,
+              const __grid_constant__ CUtensorMap kv_map, const int32_t* __restrict__ block_table,
               const int32_t* __restrict__ seq_lens, float scale_log2e, int Hq, int Hk,
               int QG, int num_blocks, int max_blocks, int S, Workspace ws,
               unsigned* __restrict__ err) {
@@ -301,20 +306,16 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
       const uint32_t bar = bar_base + 8 * stg;
       const bool ok = (unsigned)pid < (unsigned)num_blocks;
       stage_ok = ok ? (stage_ok | (1u << stg)) : (stage_ok & ~(1u << stg));
-      fence_proxy_async_smem();
-      __syncwarp();
+      // the warp has finished reading this stage (callers __syncwarp first)
       if (lane == 0) {
         if (ok) {
+          fence_proxy_async_smem();
           mbar_arrive_expect_tx(bar, kTileBytes);
+          tma_load_3d(stage_base + stg * kTileBytes, &kv_map, 0, g, pid * kPage, bar);
         } else {
           atomicOr(err, kErrBadPage);
           mbar_arrive(bar);
         }
-      }
-      __syncwarp();
-      if (ok && lane < kPage) {
-        const uint8_t* src = kv + (((int64_t)pid * kPage + lane) * Hk + g) * (int64_t)kSlotBytes;
-        bulk_g2s(stage_base + stg * kTileBytes + lane * kSlotBytes, src, kSlotBytes, bar);
       }
     };
 
@@ -736,6 +737,30 @@ static cudaError_t stage1_grid(int* grid) {
   return cudaSuccess;
 }
 
+// The cache as a 3-D tensor of 32-bit words: x = word within a slot (68),
+// y = kv head (Hk, stride 272 B), z = slot (num_blocks * 16, stride Hk * 272 B).
+// One box of 68 x 1 x 16 words is one (page, kv head) tile.
+static cudaError_t make_kv_tensor_map(CUtensorMap* map, const uint8_t* kv, int Hk, int num_blocks) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const cuuint64_t dims[3] = {kSlotBytes / 4, (cuuint64_t)Hk, (cuuint64_t)num_blocks * kPage};
+  const cuuint64_t strides[2] = {kSlotBytes, (cuuint64_t)Hk * kSlotBytes};
+  const cuuint32_t box[3] = {kSlotBytes / 4, 1, kPage};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint8_t*>(kv), dims,
+                      strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int NT>
 static cudaError_t launch_stage1_t(const uint16_t* query, int64_t q_ss, int64_t q_sh,
                                    const uint8_t* kv, const int32_t* bt, const int32_t* sl,
@@ -747,11 +772,13 @@ static cudaError_t launch_stage1_t(const uint16_t* query, int64_t q_ss, int64_t 
   int grid = 0;
   cudaError_t e = stage1_grid<NT>(&grid);
   if (e != cudaSuccess) return e;
+  CUtensorMap kv_map;
+  if ((e = make_kv_tensor_map(&kv_map, kv, Hk, num_blocks)) != cudaSuccess) return e;
   decode_plan<<<1, kPlanThreads, 0, stream>>>(sl, B, Hk, S, max_blocks, grid * kUnitsPerCta, ws);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (ev_before && (e = record_timing_event(ev_before, stream)) != cudaSuccess) return e;
   decode_stage1<NT, NWARPS, NSTAGE><<<grid, NWARPS * 32, Lay::kBytes, stream>>>(
-      query, q_ss, q_sh, kv, bt, sl, scale * kLog2e, Hq, Hk, Hq / Hk, num_blocks, max_blocks, S,
+      query, q_ss, q_sh, kv_map, bt, sl, scale * kLog2e, Hq, Hk, Hq / Hk, num_blocks, max_blocks, S,
       ws, err);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (ev_after && (e = record_timing_event(ev_after, stream)) != cudaSuccess) return e;
