@@ -352,11 +352,11 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
             }
 #pragma unroll
         for (int m = 1; m < 32; m <<= 1) {
-          const bool upper = (lane & m) != 0;
+          const float sgn = (lane & m) ? -1.f : 1.f;   // upper lane: other - own
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const float other = __shfl_xor_sync(0xffffffffu, x[i], m);
-            x[i] = upper ? (other - x[i]) : (x[i] + other);
+            x[i] = fmaf(x[i], sgn, other);
           }
         }
 #pragma unroll

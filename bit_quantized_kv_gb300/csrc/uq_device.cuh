@@ -29,15 +29,19 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) {
   return __uint_as_float(bits16 << 16);
 }
 
-// Two fp32 -> one byte of two E2M1 codes: `lo` in bits 0-3, `hi` in bits 4-7.
-// Round to nearest even, saturating at +-6 (cvt ... satfinite).  The sign bit
-// of each nibble is then forced to the sign of its input, so a negative value
-// that rounds to zero is stored with its sign.
-__device__ __forceinline__ uint32_t e2m1x2_from_f32(float lo, float hi) {
+// Eight fp32 -> one word of eight E2M1 codes, element i in nibble i (bits
+// 4i..4i+3).  Round to nearest even, saturating at +-6 (cvt ... satfinite);
+// the conversion keeps the sign bit of a negative value that rounds to zero.
+__device__ __forceinline__ uint32_t e2m1x8_from_f32(const float (&y)[8]) {
   uint32_t r;
-  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n}\n"
-      : "=r"(r) : "f"(hi), "f"(lo));
-  r |= ((__float_as_uint(lo) >> 28) & 0x8u) | ((__float_as_uint(hi) >> 24) & 0x80u);
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n}\n"
+      : "=r"(r)
+      : "f"(y[0]), "f"(y[1]), "f"(y[2]), "f"(y[3]), "f"(y[4]), "f"(y[5]), "f"(y[6]), "f"(y[7]));
   return r;
 }
 

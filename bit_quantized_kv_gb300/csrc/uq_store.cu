@@ -35,12 +35,13 @@ __device__ __forceinline__ void fwht256_group8(float (&x)[32], int glane) {
   }
 #pragma unroll
   for (int m = 1; m < kLanesPerRow; m <<= 1) {
-    const bool upper = (glane & m) != 0;
+    // lower lane holds a (own), upper lane holds b (own): (a + b, a - b).
+    // fma(own, -1, other) rounds other - own exactly like a subtraction.
+    const float sgn = (glane & m) ? -1.f : 1.f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      float other = __shfl_xor_sync(0xffffffffu, x[i], m);
-      // lower lane holds a (own), upper lane holds b (own): (a + b, a - b)
-      x[i] = upper ? (other - x[i]) : (x[i] + other);
+      const float other = __shfl_xor_sync(0xffffffffu, x[i], m);
+      x[i] = fmaf(x[i], sgn, other);
     }
   }
 }
@@ -58,13 +59,10 @@ __device__ __forceinline__ uint32_t quantize_block32(const float (&x)[32], uint4
   uint32_t w[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    uint32_t acc = 0;
+    float y[8];
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {
-      const int e = q * 8 + p * 2;
-      acc |= e2m1x2_from_f32(x[e] * inv, x[e + 1] * inv) << (8 * p);
-    }
-    w[q] = acc;
+    for (int e = 0; e < 8; ++e) y[e] = x[q * 8 + e] * inv;
+    w[q] = e2m1x8_from_f32(y);
   }
   codes = make_uint4(w[0], w[1], w[2], w[3]);
   return byte;

@@ -101,6 +101,8 @@ def decode_workload(name: str) -> DecodeWorkload:
                   outlier K channels
     skewed        B=128, Hq=64, Hk=4 (GQA 16), L = floor(exp(U(ln 128, ln 131072))),
                   max_model_len 131072, S=32, seed 3, CUDA-graph replay
+    outlier_ncu   B=16, Hq=48, Hk=8, L=16384 each, outlier K: the outlier shape at a
+                  size a full ncu capture can replay (570 MB of cache)
     All use D=256, block_size=16, scale=1/16, bf16 q/K/V ~ N(0,1).
     """
     if name == "tiny":
@@ -114,6 +116,11 @@ def decode_workload(name: str) -> DecodeWorkload:
         lens = rng.integers(16384, 32768 + 1, size=64)
         return make_decode_workload("outlier_long", 64, 48, 8, lens, 32768 // BLOCK_SIZE, 32,
                                     seed=2, outliers=True)
+    if name == "outlier_ncu":
+        # the outlier workload's shape at 16 sequences of 16384 tokens (570 MB
+        # of cache, above L2, small enough for a full ncu capture)
+        return make_decode_workload("outlier_ncu", 16, 48, 8, np.full(16, 16384), 16384 // BLOCK_SIZE,
+                                    32, seed=2, outliers=True)
     if name == "skewed":
         rng = np.random.default_rng(3)
         lens = np.floor(np.exp(rng.uniform(math.log(128), math.log(131072), size=128)))
@@ -123,7 +130,7 @@ def decode_workload(name: str) -> DecodeWorkload:
     raise KeyError(name)
 
 
-DECODE_WORKLOADS = ("tiny", "batch", "outlier_long", "skewed")
+DECODE_WORKLOADS = ("tiny", "batch", "outlier_long", "skewed", "outlier_ncu")
 
 
 def _gen(device, seed: int) -> torch.Generator:
