@@ -328,7 +328,7 @@ def run_gpu(args, rank, local, world):
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "stage1_ms": round(s1_ms, 5), "stage1_bytes": kv_bytes},
         "e2e": e2e,
-        "gpu_launches": n * 3,
+        "gpu_launches": n * 4,   # per step: store, plan, stage 1, stage 2
         "clocks": clocks_sum,
     }
     if rank == 0 and not args.no_cpu_baseline:
