@@ -41,7 +41,8 @@ sys.path.insert(0, ROOT)
 METRIC = "FP4-KV decode attn: achieved HBM GB/s (% of peak), decode tokens/s"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["bit_quantized_kv_gb300/csrc/uq_decode.cu", "bit_quantized_kv_gb300/csrc/uq_device.cuh"]
+KERNEL_SOURCES = ["bit_quantized_kv_gb300/csrc/uq_decode.cu", "bit_quantized_kv_gb300/csrc/uq_decode_common.cuh",
+                  "bit_quantized_kv_gb300/csrc/uq_device.cuh"]
 
 
 def _peaks():

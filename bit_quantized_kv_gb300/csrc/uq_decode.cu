@@ -40,75 +40,9 @@
 //
 // Stage 2: one warp per (sequence, query head) merges the active splits with
 // the log-sum-exp rule and writes bf16.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include "uq_device.cuh"
+#include "uq_decode_common.cuh"
 
 namespace uq {
-
-constexpr int kPage = 16;                        // tokens per page (block_size)
-constexpr int kTileBytes = kPage * kSlotBytes;   // 4352 bytes per (page, kv head)
-#ifndef UQ_MIN_PAGES_PER_UNIT
-#define UQ_MIN_PAGES_PER_UNIT 8
-#endif
-#ifndef UQ_UNITS_PER_CTA
-#define UQ_UNITS_PER_CTA 4
-#endif
-#ifndef UQ_S1_NSTAGE
-#define UQ_S1_NSTAGE 2
-#endif
-#ifndef UQ_S1_MIN_BLOCKS
-#define UQ_S1_MIN_BLOCKS 4
-#endif
-constexpr int kMinPagesPerUnit = UQ_MIN_PAGES_PER_UNIT;  // floor of 128 tokens per split
-constexpr int kUnitsPerCta = UQ_UNITS_PER_CTA;           // work units per resident CTA
-constexpr int kStage1Stages = UQ_S1_NSTAGE;              // pages in flight per warp
-constexpr int kPlanThreads = 1024;
-constexpr float kLog2e = 1.4426950408889634f;
-
-// ---------------------------------------------------------------------------
-// Workspace layout (caller-owned, no initialisation needed).
-// ---------------------------------------------------------------------------
-struct Workspace {
-  float* part_o;       // [B][Hq][S][256] split outputs, normalised
-  float* part_lse;     // [B][Hq][S]      log2-sum-exp of each split
-  uint32_t* units;     // [<= S * B * Hk] b | split << 16 | kv_head << 24
-  int2* seq_info;      // [B] (pages per split, active splits)
-  int* order;          // [B] sequences with at least one page, longest split first
-  int* hdr;            // [0] number of units, [1] next unit to take
-};
-
-__host__ __device__ inline size_t workspace_bytes(int B, int Hq, int S) {
-  const size_t rows = (size_t)B * Hq * S;
-  const size_t bytes = rows * kHeadDim * 4 + rows * 4 + rows * 4 + (size_t)B * 8 +
-                       (size_t)B * 4 + 64;
-  return (bytes + 255) / 256 * 256;
-}
-
-__host__ __device__ inline Workspace workspace_layout(void* base, int B, int Hq, int S) {
-  const size_t rows = (size_t)B * Hq * S;
-  uint8_t* p = static_cast<uint8_t*>(base);
-  Workspace w;
-  w.part_o = reinterpret_cast<float*>(p);
-  p += rows * kHeadDim * 4;
-  w.part_lse = reinterpret_cast<float*>(p);
-  p += rows * 4;
-  w.units = reinterpret_cast<uint32_t*>(p);
-  p += rows * 4;
-  w.seq_info = reinterpret_cast<int2*>(p);   // rows * 1032 is a multiple of 8
-  p += (size_t)B * 8;
-  w.order = reinterpret_cast<int*>(p);
-  p += (size_t)B * 4;
-  w.hdr = reinterpret_cast<int*>(p);
-  return w;
-}
-
-__device__ __forceinline__ int clamp_len(int L, int max_blocks) {
-  L = max(L, 0);
-  const long long cap = (long long)max_blocks * kPage;
-  return (long long)L > cap ? (int)cap : L;
-}
 
 // ---------------------------------------------------------------------------
 // Plan.
@@ -232,12 +166,6 @@ struct Stage1Layout {
   static constexpr int kQBytes = kRows * kQRowBytes;
   static constexpr int kBytes = kQOff + kQBytes;
 };
-
-__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1,
-                                            uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
-}
 
 template <int NT, int NWARPS, int NSTAGE>
 __global__ void __launch_bounds__(NWARPS * 32, NT == 1 ? UQ_S1_MIN_BLOCKS : 2)
@@ -470,11 +398,14 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
         const float evf0 = __uint_as_float(lds32(meta_f + (kPage + gq) * 4));
         const float evf1 = __uint_as_float(lds32(meta_f + (kPage + gq + 8) * 4));
 
-        // -- scores and online softmax
+        // -- scores and online softmax.  Both running maxima move lazily: only
+        //    when a page's maximum exceeds the reference by more than
+        //    kLazyMaxLog2, so a probability stays below 2^kLazyMaxLog2 (f16 keeps
+        //    its full relative precision there) and rescaling O is rare.
         const bool v0 = gq < nvalid, v1 = gq + 8 < nvalid;
         uint32_t pw[NT][2];
         bool rescale = false;
-        float alpha_o[NT][2];
+        float mu_prev[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           float sres[4];
@@ -498,12 +429,13 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
               tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, msk));
               umax = fmaxf(umax, __shfl_xor_sync(0xffffffffu, umax, msk));
             }
-            const float m_new = fmaxf(m_run[nt][h], tmax);
-            const float mu_new = fmaxf(mu_run[nt][h], umax);
-            l_run[nt][h] = l_run[nt][h] * fast_exp2(m_run[nt][h] - m_new) + fast_exp2(s0 - m_new) +
+            const float m_old = m_run[nt][h], mu_old = mu_run[nt][h];
+            const float m_new = tmax > m_old + kLazyMaxLog2 ? tmax : m_old;
+            const float mu_new = umax > mu_old + kLazyMaxLog2 ? umax : mu_old;
+            l_run[nt][h] = l_run[nt][h] * fast_exp2(m_old - m_new) + fast_exp2(s0 - m_new) +
                            fast_exp2(s1 - m_new);
-            alpha_o[nt][h] = fast_exp2(mu_run[nt][h] - mu_new);
-            rescale |= mu_new != mu_run[nt][h];
+            mu_prev[nt][h] = mu_old;
+            rescale |= mu_new != mu_old;
             m_run[nt][h] = m_new;
             mu_run[nt][h] = mu_new;
             w4[h] = fast_exp2(u0 - mu_new);
@@ -514,14 +446,17 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
         }
         if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
+          for (int nt = 0; nt < NT; ++nt) {
+            const float a0 = fast_exp2(mu_prev[nt][0] - mu_run[nt][0]);
+            const float a1 = fast_exp2(mu_prev[nt][1] - mu_run[nt][1]);
 #pragma unroll
             for (int mt = 0; mt < 16; ++mt) {
-              o[nt][mt][0] *= alpha_o[nt][0];
-              o[nt][mt][1] *= alpha_o[nt][1];
-              o[nt][mt][2] *= alpha_o[nt][0];
-              o[nt][mt][3] *= alpha_o[nt][1];
+              o[nt][mt][0] *= a0;
+              o[nt][mt][1] *= a1;
+              o[nt][mt][2] *= a0;
+              o[nt][mt][3] *= a1;
             }
+          }
         }
         // -- PV on the tensor cores
         const uint32_t voff = kVCodeOff + 16 * gq;
@@ -761,12 +696,14 @@ static cudaError_t make_kv_tensor_map(CUtensorMap* map, const uint8_t* kv, int H
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Plan, then stage 1 (bracketed by the caller's timing events, if any).
 template <int NT>
-static cudaError_t launch_stage1_t(const uint16_t* query, int64_t q_ss, int64_t q_sh,
-                                   const uint8_t* kv, const int32_t* bt, const int32_t* sl,
-                                   float scale, int B, int Hq, int Hk, int num_blocks,
-                                   int max_blocks, int S, const Workspace& ws, unsigned* err,
-                                   cudaStream_t stream, cudaEvent_t ev_before, cudaEvent_t ev_after) {
+static cudaError_t launch_plan_and_stage1(const uint16_t* query, int64_t q_ss, int64_t q_sh,
+                                          const uint8_t* kv, const int32_t* bt, const int32_t* sl,
+                                          float scale, int B, int Hq, int Hk, int num_blocks,
+                                          int max_blocks, int S, const Workspace& ws, unsigned* err,
+                                          cudaStream_t stream, cudaEvent_t ev_before,
+                                          cudaEvent_t ev_after) {
   constexpr int NWARPS = 4, NSTAGE = kStage1Stages;
   using Lay = Stage1Layout<NT, NWARPS, NSTAGE>;
   int grid = 0;
@@ -793,10 +730,12 @@ cudaError_t launch_decode(const uint16_t* query, int64_t q_ss, int64_t q_sh, con
                           uint16_t* out, unsigned* err, cudaStream_t stream,
                           cudaEvent_t ev_before_stage1, cudaEvent_t ev_after_stage1) {
   const Workspace ws = workspace_layout(workspace, B, Hq, S);
-  const int QG = Hq / Hk;
-  cudaError_t e = (QG == 16)
-      ? launch_stage1_t<2>(query, q_ss, q_sh, kv, bt, sl, scale, B, Hq, Hk, num_blocks, max_blocks, S, ws, err, stream, ev_before_stage1, ev_after_stage1)
-      : launch_stage1_t<1>(query, q_ss, q_sh, kv, bt, sl, scale, B, Hq, Hk, num_blocks, max_blocks, S, ws, err, stream, ev_before_stage1, ev_after_stage1);
+  cudaError_t e =
+      (Hq / Hk == 16)
+          ? launch_plan_and_stage1<2>(query, q_ss, q_sh, kv, bt, sl, scale, B, Hq, Hk, num_blocks,
+                                      max_blocks, S, ws, err, stream, ev_before_stage1, ev_after_stage1)
+          : launch_plan_and_stage1<1>(query, q_ss, q_sh, kv, bt, sl, scale, B, Hq, Hk, num_blocks,
+                                      max_blocks, S, ws, err, stream, ev_before_stage1, ev_after_stage1);
   if (e != cudaSuccess) return e;
   const int rows = B * Hq;
   decode_stage2<<<(rows + 3) / 4, 128, 0, stream>>>(ws, B, Hq, S, out);

@@ -1,0 +1,85 @@
+// uq_decode_common.cuh -- definitions shared by the decode kernels: page
+// geometry and the caller-owned workspace layout (split partials and the
+// device-side plan).
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "uq_device.cuh"
+
+namespace uq {
+
+constexpr int kPage = 16;                        // tokens per page (block_size)
+constexpr int kTileBytes = kPage * kSlotBytes;   // 4352 bytes per (page, kv head)
+#ifndef UQ_MIN_PAGES_PER_UNIT
+#define UQ_MIN_PAGES_PER_UNIT 8
+#endif
+#ifndef UQ_UNITS_PER_CTA
+#define UQ_UNITS_PER_CTA 4
+#endif
+#ifndef UQ_S1_NSTAGE
+#define UQ_S1_NSTAGE 2
+#endif
+#ifndef UQ_S1_MIN_BLOCKS
+#define UQ_S1_MIN_BLOCKS 4
+#endif
+constexpr int kMinPagesPerUnit = UQ_MIN_PAGES_PER_UNIT;  // floor of 128 tokens per split
+constexpr int kUnitsPerCta = UQ_UNITS_PER_CTA;           // work units per resident CTA
+constexpr int kStage1Stages = UQ_S1_NSTAGE;              // pages in flight per warp
+constexpr int kPlanThreads = 1024;
+constexpr float kLog2e = 1.4426950408889634f;
+// A running softmax maximum (log2 units) moves only when a page's maximum
+// exceeds it by more than this, so probabilities stay below 2^8.
+constexpr float kLazyMaxLog2 = 8.f;
+
+// ---------------------------------------------------------------------------
+// Workspace layout (caller-owned, no initialisation needed).
+// ---------------------------------------------------------------------------
+struct Workspace {
+  float* part_o;       // [B][Hq][S][256] split outputs, normalised
+  float* part_lse;     // [B][Hq][S]      log2-sum-exp of each split
+  uint32_t* units;     // [<= S * B * Hk] b | split << 16 | kv_head << 24
+  int2* seq_info;      // [B] (pages per split, active splits)
+  int* order;          // [B] sequences with at least one page, longest split first
+  int* hdr;            // [0] number of units, [1] next unit to take
+};
+
+__host__ __device__ inline size_t workspace_bytes(int B, int Hq, int S) {
+  const size_t rows = (size_t)B * Hq * S;
+  const size_t bytes = rows * kHeadDim * 4 + rows * 4 + rows * 4 + (size_t)B * 8 +
+                       (size_t)B * 4 + 64;
+  return (bytes + 255) / 256 * 256;
+}
+
+__host__ __device__ inline Workspace workspace_layout(void* base, int B, int Hq, int S) {
+  const size_t rows = (size_t)B * Hq * S;
+  uint8_t* p = static_cast<uint8_t*>(base);
+  Workspace w;
+  w.part_o = reinterpret_cast<float*>(p);
+  p += rows * kHeadDim * 4;
+  w.part_lse = reinterpret_cast<float*>(p);
+  p += rows * 4;
+  w.units = reinterpret_cast<uint32_t*>(p);
+  p += rows * 4;
+  w.seq_info = reinterpret_cast<int2*>(p);   // rows * 1032 is a multiple of 8
+  p += (size_t)B * 8;
+  w.order = reinterpret_cast<int*>(p);
+  p += (size_t)B * 4;
+  w.hdr = reinterpret_cast<int*>(p);
+  return w;
+}
+
+__device__ __forceinline__ int clamp_len(int L, int max_blocks) {
+  L = max(L, 0);
+  const long long cap = (long long)max_blocks * kPage;
+  return (long long)L > cap ? (int)cap : L;
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                            uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+
+}  // namespace uq

@@ -132,8 +132,9 @@ def test_cuda_graph_replay_with_new_lengths():
     assert binding.uq_check_device_error() == 0
 
 
-def test_bad_page_id_is_flagged_and_skipped():
-    wl = workloads.make_decode_workload("bad", 2, 8, 1, np.array([64, 64]), 4, 2, seed=43)
+@pytest.mark.parametrize("Hq", [8, 16])
+def test_bad_page_id_is_flagged_and_skipped(Hq):
+    wl = workloads.make_decode_workload("bad", 2, Hq, 1, np.array([64, 64]), 4, 2, seed=43)
     cache = fill_cache_gpu(wl)
     q = workloads.query(wl, "cuda")
     bt = wl.block_table.copy()
