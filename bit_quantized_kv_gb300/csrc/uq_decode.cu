@@ -13,13 +13,9 @@
 // of whole pages.  Units (sequence, split, kv head) are listed with the
 // longest units first; the plan also resets the unit counter.
 //
-// Stage 1 (persistent: resident CTAs only, 8 warps each).  Each CTA takes
-// units from the counter and walks a unit in groups of 8 pages, one page per
-// warp.  QK of a group (128 tokens x 16 query rows) is one set of 8
-// block-scaled tcgen05 MMAs (kind::mxf8f6f4: K codes as E2M1 with their UE8M0
-// block scales in tensor memory, q' as E4M3), issued by one thread after the
-// warps have copied their pages' K codes into the padded operand layout; each
-// warp keeps its own online-softmax state; a page's 16 slots of one kv head
+// Stage 1 (persistent: resident CTAs only, 4 warps each).  Each CTA takes
+// units from the counter.  Inside a unit each warp takes every 4th page and
+// keeps its own online-softmax state; a page's 16 slots of one kv head
 // (16 x 272 B, strided by Hk * 272 B in the cache) arrive in shared memory as
 // one TMA tile copy (a 3-D tensor map over the cache: 68 words x Hk heads x
 // slots, box 68 x 1 x 16) completing on a per-stage mbarrier, NSTAGE pages
@@ -145,79 +141,55 @@ decode_plan(const int32_t* __restrict__ seq_lens, int B, int Hk, int S, int max_
 // ---------------------------------------------------------------------------
 // Stage 1.
 // ---------------------------------------------------------------------------
-constexpr int kS1Warps = 8;                      // one page per warp in each group
-constexpr int kGroupRows = kS1Warps * kPage;     // 128 tokens: M of the QK MMA
-constexpr int kQkN = 16;                         // N of the QK MMA: query rows, zero padded
-// tensor-memory columns of a CTA: scores [0, 16), K block scales [16, 24),
-// query block scales [24, 32)
-constexpr uint32_t kTmemCols = 32, kTmemD = 0, kTmemSfa = 16, kTmemSfb = 24;
-// QK instruction descriptor (kind::mxf8f6f4, block scaled): A = K codes E2M1,
-// B = q' E4M3, both K-major, UE8M0 scales, N = 16, M = 128.
-constexpr uint32_t kQkIdesc = (5u << 7) | (0u << 10) | ((uint32_t)(kQkN >> 3) << 17) | (1u << 23) |
-                              ((uint32_t)(kGroupRows >> 4) << 24);
-// A operand: row r (token), 16-element chunk k (8 code bytes + 8 zero bytes)
-// at k * kAChunkStride + (r / 8) * 128 + (r % 8) * 16.
-constexpr int kAChunkStride = kGroupRows / 8 * 128;   // 2048
-// B operand: row n, 16-byte chunk k (16 head dims) at k * 256 + (n / 8) * 128 + (n % 8) * 16.
-constexpr int kBChunkStride = kQkN / 8 * 128;         // 256
-
-template <int NT>
+template <int NT, int NWARPS, int NSTAGE>
 struct Stage1Layout {
-  static constexpr int kRows = NT * 8;                       // query rows of a warp's state
-  static constexpr int kStageBytes = kS1Warps * kStage1Stages * kTileBytes;
+  static constexpr int kRows = NT * 8;                       // padded query rows
+  static constexpr int kStageBytes = NWARPS * NSTAGE * kTileBytes;
   static constexpr int kORowStride = kHeadDim + 4;           // floats
-  static constexpr int kMergeBytes = kS1Warps * kRows * kORowStride * 4;
+  static constexpr int kMergeBytes = NWARPS * kRows * kORowStride * 4;
   static constexpr int kUnionBytes = kStageBytes > kMergeBytes ? kStageBytes : kMergeBytes;
-  static constexpr int kAOff = (kUnionBytes + 1023) / 1024 * 1024;
-  static constexpr int kABytes = kGroupRows * kHeadDim;      // 32 KB
-  static constexpr int kBOff = kAOff + kABytes;
-  static constexpr int kBBytes = kQkN * kHeadDim;            // 4 KB
-  static constexpr int kStatsOff = kBOff + kBBytes;          // [warp][row][4] floats
-  static constexpr int kStatsBytes = kS1Warps * kRows * 16;
-  static constexpr int kRowInfoOff = kStatsOff + kStatsBytes; // [row][warps + 2] floats
-  static constexpr int kRowInfoBytes = kRows * (kS1Warps + 2) * 4;
+  static constexpr int kStatsOff = kUnionBytes;              // [NWARPS][kRows][4] floats
+  static constexpr int kStatsBytes = NWARPS * kRows * 4 * 4;
+  static constexpr int kRowInfoOff = kStatsOff + kStatsBytes; // [kRows][NWARPS+2] floats
+  static constexpr int kRowInfoBytes = kRows * (NWARPS + 2) * 4;
   static constexpr int kLutOff = (kRowInfoOff + kRowInfoBytes + 15) / 16 * 16;
   static constexpr int kLutBytes = 256 * 4;                  // 2^-delta as f16x2
-  // per warp, per page: [token] 8 relative V block scales (f16), then [token]
-  // the V exponent factor (fp32)
-  static constexpr int kMetaRelBytes = kPage * 16;
-  static constexpr int kMetaWarpBytes = kMetaRelBytes + kPage * 4;
+  // per warp, per tile: [K, V][token] 8 relative block scales (f16) and one factor
+  static constexpr int kMetaRelBytes = 2 * kPage * 16;
+  static constexpr int kMetaWarpBytes = kMetaRelBytes + 2 * kPage * 4;
   static constexpr int kMetaOff = kLutOff + kLutBytes;
-  static constexpr int kBarOff = kMetaOff + kS1Warps * kMetaWarpBytes;
-  static constexpr int kBarBytes = kS1Warps * kStage1Stages * 8 + 8;   // page barriers, MMA barrier
-  static constexpr int kMiscOff = kBarOff + kBarBytes;       // [0] unit, [1] stop, [2] TMEM base
-  static constexpr int kBytes = kMiscOff + 16;
+  static constexpr int kBarOff = kMetaOff + NWARPS * kMetaWarpBytes;
+  static constexpr int kBarBytes = NWARPS * NSTAGE * 8;
+  static constexpr int kMiscOff = kBarOff + kBarBytes;       // unit id, abort flag
+  static constexpr int kQOff = (kMiscOff + 16 + 127) / 128 * 128;
+  static constexpr int kQRowBytes = kHeadDim * 2 + 16;       // padded: conflict-free ldmatrix
+  static constexpr int kQBytes = kRows * kQRowBytes;
+  static constexpr int kBytes = kQOff + kQBytes;
 };
 
-template <int NT>
-__global__ void __launch_bounds__(kS1Warps * 32, NT == 1 ? 2 : 1)
+template <int NT, int NWARPS, int NSTAGE>
+__global__ void __launch_bounds__(NWARPS * 32, NT == 1 ? UQ_S1_MIN_BLOCKS : 2)
 decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
               const __grid_constant__ CUtensorMap kv_map, const int32_t* __restrict__ block_table,
               const int32_t* __restrict__ seq_lens, float scale_log2e, int Hq, int Hk,
               int QG, int num_blocks, int max_blocks, int S, Workspace ws,
               unsigned* __restrict__ err) {
-  using Lay = Stage1Layout<NT>;
-  constexpr int NSTAGE = kStage1Stages;
-  constexpr int NWARPS = kS1Warps;
-  extern __shared__ __align__(1024) uint8_t smem[];
+  using Lay = Stage1Layout<NT, NWARPS, NSTAGE>;
+  constexpr int NCH = NT == 1 ? 4 : 2;   // independent QK accumulator chains per n-tile
+  extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, c = lane & 3;
   const uint32_t smem_base = smem_u32(smem);
   const uint32_t bar_base = smem_base + Lay::kBarOff + warp * NSTAGE * 8;
-  const uint32_t mma_bar = smem_base + Lay::kBarOff + NWARPS * NSTAGE * 8;
   const uint32_t stage_base = smem_base + warp * NSTAGE * kTileBytes;
-  const uint32_t a_base = smem_base + Lay::kAOff;
-  const uint32_t b_base = smem_base + Lay::kBOff;
   const uint32_t lut_base = smem_base + Lay::kLutOff;
   const uint32_t meta_rel = smem_base + Lay::kMetaOff + warp * Lay::kMetaWarpBytes;
   const uint32_t meta_f = meta_rel + Lay::kMetaRelBytes;
   volatile int* s_misc = reinterpret_cast<volatile int*>(smem + Lay::kMiscOff);
-  // this warp's 16 rows of the group MMA = its tensor-memory lanes
-  const int row0 = 32 * (warp & 3) + 16 * (warp >> 2);
+  uint16_t* qs = reinterpret_cast<uint16_t*>(smem + Lay::kQOff);
 
-  if (warp == 0) tmem_alloc(smem_base + Lay::kMiscOff + 8, kTmemCols);
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NWARPS * NSTAGE + 1; ++i) mbar_init(smem_base + Lay::kBarOff + 8 * i, 1);
+    for (int i = 0; i < NWARPS * NSTAGE; ++i) mbar_init(smem_base + Lay::kBarOff + 8 * i, 1);
     s_misc[1] = 0;
     fence_barrier_init();
   }
@@ -225,20 +197,11 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
     const uint32_t h = pow2_neg_f16(i);
     reinterpret_cast<uint32_t*>(smem + Lay::kLutOff)[i] = h | (h << 16);
   }
-  // A operand padding stays zero from here on
-  for (int i = threadIdx.x; i < Lay::kABytes / 16; i += NWARPS * 32) sts128(a_base + 16 * i, make_uint4(0u, 0u, 0u, 0u));
-  tc_fence_before_sync();
   __syncthreads();
-  tc_fence_after_sync();
-  const uint32_t tmem = (uint32_t)s_misc[2];
-  const uint32_t tmem_rows = tmem + ((uint32_t)row0 << 16);
-  // the query side has no block scales: 2^0 everywhere
-  tmem_st_16x256b(tmem_rows + kTmemSfb, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
 
   const int n_units = ws.hdr[0];
-  uint32_t tiles_done = 0;   // this warp's pages so far: drives stage and parity
+  uint32_t tiles_done = 0;   // this warp's tiles so far: drives stage and parity
   uint32_t stage_ok = 0;     // bit s: stage s holds a page that was really copied
-  uint32_t mma_phase = 0;
   const int ta = 2 * c, tb = 2 * c + 1, tcc = 2 * c + 8, td = 2 * c + 9;
 
   for (;;) {
@@ -254,12 +217,11 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
     const int p_begin = split * pps;
     const int p_end = min(p_begin + pps, P);
 
-    // ---- page schedule: group j holds pages p_begin + 8j .. +7, warp w the w-th
+    // ---- per-warp page schedule ---------------------------------------------
     const int n_pages = p_end - p_begin;
-    const int n_groups = (n_pages + NWARPS - 1) / NWARPS;
     const int n_my = n_pages > warp ? (n_pages - warp + NWARPS - 1) / NWARPS : 0;
     const int32_t* bt_row = block_table + (int64_t)b * max_blocks + p_begin + warp;
-    int pid_chunk = -1, pid_reg = -1, issued = 0;
+    int pid_chunk = -1, pid_reg = -1;
 
     auto issue = [&](int j, int stg) {
       const int chunk = j >> 5;
@@ -283,16 +245,20 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
           mbar_arrive(bar);
         }
       }
-      ++issued;
     };
 
+    // this unit's first tile lands in stage tiles_done % NSTAGE, phase parity
+    // (tiles_done / NSTAGE) & 1; later tiles advance both incrementally
     const int stg0 = (int)(tiles_done % NSTAGE);
     const uint32_t ph0 = (tiles_done / NSTAGE) & 1u;
     for (int j = 0; j < NSTAGE && j < n_my; ++j) issue(j, (stg0 + j) % NSTAGE);
 
-    // ---- query prologue: B operand q' = e4m3(fp32(q) H), rows >= QG zero -------
-    for (int r = warp; r < kQkN; r += NWARPS) {
-      uint32_t w0 = 0u, w1 = 0u;
+    // ---- query prologue: q' = f16(e4m3(fp32(q) H)) in operand order -----------
+    // Row r, k-step i, position kp holds head dim 64c + 4i + e with
+    // kp = 2c + (e & 1) + 8 (e >> 1).
+    for (int r = warp; r < Lay::kRows; r += NWARPS) {
+      uint8_t* row = reinterpret_cast<uint8_t*>(qs) + r * Lay::kQRowBytes;
+      uint32_t pk[4] = {0u, 0u, 0u, 0u};
       if (r < QG) {
         const uint16_t* qp = query + (int64_t)b * q_ss + (int64_t)(g * QG + r) * q_sh + lane * 8;
         const uint4 raw = *reinterpret_cast<const uint4*>(qp);
@@ -321,14 +287,24 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
             x[i] = fmaf(x[i], sgn, other);
           }
         }
-        w0 = e4m3x4_from_f32(x[0] * 0.0625f, x[1] * 0.0625f, x[2] * 0.0625f, x[3] * 0.0625f);
-        w1 = e4m3x4_from_f32(x[4] * 0.0625f, x[5] * 0.0625f, x[6] * 0.0625f, x[7] * 0.0625f);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) pk[i] = e4m3_roundtrip_f16x2(x[2 * i] * 0.0625f, x[2 * i + 1] * 0.0625f);
       }
-      // lane holds head dims 8 lane .. 8 lane + 7: chunk lane / 2, bytes 8 (lane % 2) ..
-      sts64(b_base + (lane >> 1) * kBChunkStride + (r >> 3) * 128 + (r & 7) * 16 + 8 * (lane & 1), w0, w1);
+      // lane holds head dims 8*lane .. 8*lane+7: c' = lane / 8, k-steps 2(lane % 8) + {0, 1}
+      const int cq = lane >> 3, i0 = 2 * (lane & 7);
+#pragma unroll
+      for (int ii = 0; ii < 2; ++ii) {
+        uint8_t* kstep = row + (i0 + ii) * 32;
+        *reinterpret_cast<uint32_t*>(kstep + 4 * cq) = pk[2 * ii];          // kp 2c', 2c'+1
+        *reinterpret_cast<uint32_t*>(kstep + 16 + 4 * cq) = pk[2 * ii + 1]; // kp 2c'+8, 2c'+9
+      }
     }
+    __syncthreads();
 
-    // ---- main loop over the unit's page groups ------------------------------
+    // ldmatrix row addresses: lane -> matrix lane/8 (k-step +(lane>>4), half (lane>>3)&1), row lane%8
+    const uint32_t q_lds = smem_u32(qs) + (lane & 7) * Lay::kQRowBytes + (lane >> 4) * 32 + ((lane >> 3) & 1) * 16;
+
+    // ---- main loop over this warp's pages -------------------------------------
     float o[NT][16][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
@@ -345,116 +321,106 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
       }
 
     bool timed_out = false;
-    int consumed = 0;
+    int j = 0;
     int stg = stg0;
     uint32_t phase = ph0;
-    for (int j = 0; j < n_groups; ++j) {
-      const bool has = j < n_my;
-      int nvalid = 0;
-      const uint32_t sb = stage_base + stg * kTileBytes;
-      if (has && !timed_out) {
-        if (__all_sync(0xffffffffu, mbar_wait(bar_base + 8 * stg, phase))) {
-          consumed = j + 1;
-          const int page = p_begin + warp + j * NWARPS;
-          nvalid = ((stage_ok >> stg) & 1u) ? min(kPage, L - page * kPage) : 0;
-        } else {
-          timed_out = true;
-        }
+    for (; j < n_my; ++j) {
+      if (!mbar_wait(bar_base + 8 * stg, phase)) {
+        timed_out = true;
+        break;
       }
+      const int page = p_begin + warp + j * NWARPS;
+      const int nvalid = ((stage_ok >> stg) & 1u) ? min(kPage, L - page * kPage) : 0;
       if (nvalid > 0) {
-        // -- K codes -> this warp's 16 rows of the A operand (16-element chunks,
-        //    8 code bytes + 8 zero bytes each)
+        const uint32_t sb = stage_base + stg * kTileBytes;
+        // -- tile metadata, one (token, K or V) scale row per lane: the token's
+        //    largest block byte E, the 8 relative scales 2^(byte - E) as f16
+        //    and one fp32 factor (K: scale*log2e*2^(E-127); V: E-127)
         {
-          const int t = lane & 15, mh = lane >> 4;
-          const uint32_t arow = a_base + ((row0 + t) >> 3) * 128 + ((row0 + t) & 7) * 16;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int m = mh + 2 * i;   // 16 code bytes = chunks 2m, 2m+1
-            const uint4 v = lds128(sb + t * kSlotBytes + 16 * m);
-            sts128(arow + (2 * m) * kAChunkStride, make_uint4(v.x, v.y, 0u, 0u));
-            sts128(arow + (2 * m + 1) * kAChunkStride, make_uint4(v.z, v.w, 0u, 0u));
-          }
-        }
-        // -- K block scales of the same rows into tensor memory: lane = row,
-        //    columns 0..3 hold blocks 0..3 (one byte each), columns 4..7 blocks 4..7
-        {
-          const int half = c >> 1;
-          const uint32_t w1 = lds32(sb + gq * kSlotBytes + kKScaleOff + 4 * half);
-          const uint32_t w2 = lds32(sb + (gq + 8) * kSlotBytes + kKScaleOff + 4 * half);
-          tmem_st_16x256b(tmem_rows + kTmemSfa, w1, w1, w2, w2);
-        }
-        // -- V scale table: lane -> (token lane % 16, blocks 4 (lane / 16) ..); the
-        //    token's largest block byte E, 2^(byte - E) as f16, and E - 127
-        {
-          const int t = lane & 15, hf = lane >> 4;
-          const uint2 sc = lds64(sb + t * kSlotBytes + kVScaleOff);
+          const int mtok = lane & 15, kind = lane >> 4;
+          const uint2 sc = lds64(sb + mtok * kSlotBytes + kKScaleOff + 8 * kind);
           const uint32_t E = max_byte8(sc.x, sc.y);
-          const uint32_t w = hf ? sc.y : sc.x;
-          const uint32_t lE = lut_base + 4 * E;
-          const uint32_t l0 = lds32(lE - ((w << 2) & 0x3fcu)), l1 = lds32(lE - ((w >> 6) & 0x3fcu));
-          const uint32_t l2 = lds32(lE - ((w >> 14) & 0x3fcu)), l3 = lds32(lE - ((w >> 22) & 0x3fcu));
-          sts64(meta_rel + t * 16 + 8 * hf, __byte_perm(l0, l1, 0x7610), __byte_perm(l2, l3, 0x7610));
-          if (hf == 0) sts32(meta_f + t * 4, __float_as_uint((float)((int)E - 127)));
-        }
-      }
-      // -- the group's QK: 8 block-scaled MMAs (one 32-dim block each) by one thread
-      fence_proxy_async_smem();
-      tmem_wait_st();
-      tc_fence_before_sync();
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        tc_fence_after_sync();
-#pragma unroll
-        for (int kb = 0; kb < 8; ++kb) {
-          const uint64_t ad = smem_desc_noswizzle(a_base + kb * 2 * kAChunkStride, kAChunkStride, 128);
-          const uint64_t bd = smem_desc_noswizzle(b_base + kb * 2 * kBChunkStride, kBChunkStride, 128);
-          const uint32_t id = kQkIdesc | ((uint32_t)(kb & 3) << 29) | ((uint32_t)(kb & 3) << 4);
-          tc_mma_block_scaled(tmem + kTmemD, ad, bd, id, tmem + kTmemSfa + 4 * (kb >> 2),
-                              tmem + kTmemSfb + 4 * (kb >> 2), kb > 0 ? 1u : 0u);
-        }
-        tc_commit(mma_bar);
-      }
-      const bool mma_done = __all_sync(0xffffffffu, mbar_wait(mma_bar, mma_phase));
-      mma_phase ^= 1u;
-      tc_fence_after_sync();
-      if (!mma_done) {
-        if (lane == 0) atomicOr(err, kErrTimeout);
-        s_misc[1] = 1;
-        nvalid = 0;
-      }
-
-      if (nvalid > 0) {
-        // -- scores of this warp's page (tokens gq, gq+8; rows 2c, 2c+1 per n-tile)
-        float sacc[NT][4];
-        if (NT == 1) {
-          tmem_ld_16x256b_x1(tmem_rows + kTmemD, sacc[0]);
-        } else {
-          float v8[8];
-          tmem_ld_16x256b_x2(tmem_rows + kTmemD, v8);
+          uint32_t p[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            sacc[0][k] = v8[k];
-            sacc[NT - 1][k] = v8[4 + k];
+            const uint32_t w = k < 2 ? sc.x : sc.y;
+            const uint32_t b0 = (w >> (16 * (k & 1))) & 0xffu, b1 = (w >> (16 * (k & 1) + 8)) & 0xffu;
+            p[k] = (lds32(lut_base + 4 * (E - b0)) & 0xffffu) | (lds32(lut_base + 4 * (E - b1)) & 0xffff0000u);
+          }
+          sts128(meta_rel + (kind * kPage + mtok) * 16, make_uint4(p[0], p[1], p[2], p[3]));
+          const float f = kind == 0 ? scale_log2e * ue8m0_to_f32(E) : (float)((int)E - 127);
+          sts32(meta_f + (kind * kPage + mtok) * 4, __float_as_uint(f));
+        }
+        __syncwarp();
+        // K relative scales of tokens gq, gq+8 for blocks 2c, 2c+1 as f16x2 (both halves)
+        const uint32_t kr0 = lds32(meta_rel + gq * 16 + 4 * c);
+        const uint32_t kr1 = lds32(meta_rel + (gq + 8) * 16 + 4 * c);
+        const uint32_t rk0[2] = {__byte_perm(kr0, 0, 0x1010), __byte_perm(kr0, 0, 0x3232)};
+        const uint32_t rk1[2] = {__byte_perm(kr1, 0, 0x1010), __byte_perm(kr1, 0, 0x3232)};
+        // -- QK on the tensor cores, NCH independent accumulation chains
+        const uint4 ka0 = lds128(sb + gq * kSlotBytes + 32 * c);
+        const uint4 ka1 = lds128(sb + gq * kSlotBytes + 32 * c + 16);
+        const uint4 kb0 = lds128(sb + (gq + 8) * kSlotBytes + 32 * c);
+        const uint4 kb1 = lds128(sb + (gq + 8) * kSlotBytes + 32 * c + 16);
+        const uint32_t kaw[8] = {ka0.x, ka0.y, ka0.z, ka0.w, ka1.x, ka1.y, ka1.z, ka1.w};
+        const uint32_t kbw[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
+        float sacc[NT][NCH][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int ch = 0; ch < NCH; ++ch) sacc[nt][ch][0] = sacc[nt][ch][1] = sacc[nt][ch][2] = sacc[nt][ch][3] = 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          uint32_t fa[4], fb[4];
+          f16x2x4_from_e2m1_word(kaw[q], fa);
+          f16x2x4_from_e2m1_word(kbw[q], fb);
+          const uint32_t ra = rk0[q >> 2], rb = rk1[q >> 2];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            fa[e] = hmul2(fa[e], ra);
+            fb[e] = hmul2(fb[e], rb);
+          }
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            uint32_t b0, b1, b2, b3;   // k-step 2q: (b0, b1), k-step 2q+1: (b2, b3)
+            ldmatrix_x4(q_lds + nt * 8 * Lay::kQRowBytes + q * 64, b0, b1, b2, b3);
+            mma_f16_16816(sacc[nt][(2 * q) % NCH], fa[0], fb[0], fa[1], fb[1], b0, b1);
+            mma_f16_16816(sacc[nt][(2 * q + 1) % NCH], fa[2], fb[2], fa[3], fb[3], b2, b3);
           }
         }
-        const float evf0 = __uint_as_float(lds32(meta_f + gq * 4));
-        const float evf1 = __uint_as_float(lds32(meta_f + (gq + 8) * 4));
+        // -- V relative scales of tokens 2c, 2c+1, 2c+8, 2c+9 for block gq, and the
+        //    K / V factors of tokens gq, gq+8
+        const uint32_t vrel = meta_rel + kPage * 16 + 2 * gq;
+        const uint32_t rv01 = __byte_perm(lds16(vrel + ta * 16), lds16(vrel + tb * 16), 0x5410);
+        const uint32_t rv89 = __byte_perm(lds16(vrel + tcc * 16), lds16(vrel + td * 16), 0x5410);
+        const float fk0 = __uint_as_float(lds32(meta_f + gq * 4));
+        const float fk1 = __uint_as_float(lds32(meta_f + (gq + 8) * 4));
+        const float evf0 = __uint_as_float(lds32(meta_f + (kPage + gq) * 4));
+        const float evf1 = __uint_as_float(lds32(meta_f + (kPage + gq + 8) * 4));
 
-        // -- online softmax.  Both running maxima move lazily: only when a
-        //    page's maximum exceeds the reference by more than kLazyMaxLog2, so
-        //    a probability stays below 2^kLazyMaxLog2 (f16 keeps its full
-        //    relative precision there) and rescaling O is rare.
+        // -- scores and online softmax.  Both running maxima move lazily: only
+        //    when a page's maximum exceeds the reference by more than
+        //    kLazyMaxLog2, so a probability stays below 2^kLazyMaxLog2 (f16 keeps
+        //    its full relative precision there) and rescaling O is rare.
         const bool v0 = gq < nvalid, v1 = gq + 8 < nvalid;
         uint32_t pw[NT][2];
         bool rescale = false;
         float mu_prev[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
+          float sres[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            float acc = sacc[nt][0][k];
+#pragma unroll
+            for (int ch = 1; ch < NCH; ++ch) acc += sacc[nt][ch][k];
+            sres[k] = acc;
+          }
           float w4[4];
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const float s0 = v0 ? sacc[nt][h] * scale_log2e : -INFINITY;
-            const float s1 = v1 ? sacc[nt][2 + h] * scale_log2e : -INFINITY;
+            const float s0 = v0 ? sres[h] * fk0 : -INFINITY;
+            const float s1 = v1 ? sres[2 + h] * fk1 : -INFINITY;
             const float u0 = s0 + evf0;
             const float u1 = s1 + evf1;
             float tmax = fmaxf(s0, s1), umax = fmaxf(u0, u1);
@@ -492,11 +458,7 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
             }
           }
         }
-        // -- PV on the warp's tensor-core path: V relative scales of tokens 2c,
-        //    2c+1, 2c+8, 2c+9 for block gq, codes of head dims [32gq, 32gq+32)
-        const uint32_t vrel = meta_rel + 2 * gq;
-        const uint32_t rv01 = __byte_perm(lds16(vrel + ta * 16), lds16(vrel + tb * 16), 0x5410);
-        const uint32_t rv89 = __byte_perm(lds16(vrel + tcc * 16), lds16(vrel + td * 16), 0x5410);
+        // -- PV on the tensor cores
         const uint32_t voff = kVCodeOff + 16 * gq;
         const uint4 va = lds128(sb + ta * kSlotBytes + voff);
         const uint4 vb = lds128(sb + tb * kSlotBytes + voff);
@@ -527,20 +489,21 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
         }
       }
       __syncwarp();
-      if (has) {
-        if (!timed_out && j + NSTAGE < n_my) issue(j + NSTAGE, stg);   // same stage, next phase
-        if (++stg == NSTAGE) {
-          stg = 0;
-          phase ^= 1u;
-        }
+      if (j + NSTAGE < n_my) issue(j + NSTAGE, stg);   // same stage, next phase
+      if (++stg == NSTAGE) {
+        stg = 0;
+        phase ^= 1u;
       }
     }
     if (timed_out) {
       if (lane == 0) atomicOr(err, kErrTimeout);
       // wait (bounded) for this warp's copies still in flight, then stop the CTA
-      for (int jj = consumed; jj < issued; ++jj) {
-        const uint32_t t = tiles_done + (uint32_t)jj;
-        (void)mbar_wait(bar_base + 8 * (t % NSTAGE), (t / NSTAGE) & 1u);
+      for (int jj = j; jj < n_my && jj < j + NSTAGE; ++jj) {
+        (void)mbar_wait(bar_base + 8 * stg, phase);
+        if (++stg == NSTAGE) {
+          stg = 0;
+          phase ^= 1u;
+        }
       }
       s_misc[1] = 1;
 #pragma unroll
@@ -621,11 +584,8 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
       }
       *reinterpret_cast<float4*>(ws.part_o + (((int64_t)(b * Hq + g * QG + r)) * S + split) * kHeadDim + d4) = acc;
     }
-    __syncthreads();  // merge buffers (stage buffers) are free again
+    __syncthreads();  // merge buffers (stage buffers) and Q' are free again
   }
-  tc_fence_before_sync();
-  __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
 // ---------------------------------------------------------------------------
@@ -689,7 +649,8 @@ static cudaError_t record_timing_event(cudaEvent_t ev, cudaStream_t stream) {
 // persistent grid from the occupancy the kernel actually gets.
 template <int NT>
 static cudaError_t stage1_grid(int* grid) {
-  using Lay = Stage1Layout<NT>;
+  constexpr int NWARPS = 4, NSTAGE = kStage1Stages;
+  using Lay = Stage1Layout<NT, NWARPS, NSTAGE>;
   static int grid_of_device[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -698,26 +659,14 @@ static cudaError_t stage1_grid(int* grid) {
     *grid = grid_of_device[dev];
     return cudaSuccess;
   }
-  auto kern = decode_stage1<NT>;
+  auto kern = decode_stage1<NT, NWARPS, NSTAGE>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
   if (e != cudaSuccess) return e;
-  // all of L1 as shared memory, so that two 109 KB CTAs share an SM
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  int sms = 0, per_sm = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  // Resident CTAs per SM from the kernel's registers and shared memory.  The
-  // runtime's occupancy query is not used: it counts one CTA per SM for a
-  // kernel that allocates tensor memory, while this one takes 32 columns.
-  int sms = 0, smem_sm = 0, smem_reserved = 0, regs_sm = 0;
-  cudaFuncAttributes fa;
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev)) != cudaSuccess) return e;
-  if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
-  const int warp_regs = (fa.numRegs * 32 + 255) / 256 * 256;   // allocated per warp in 256-register units
-  const int by_regs = regs_sm / (warp_regs * kS1Warps);
-  const int by_smem = smem_sm / (Lay::kBytes + (int)fa.sharedSizeBytes + smem_reserved);
-  const int per_sm = by_regs < by_smem ? by_regs : by_smem;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NWARPS * 32, Lay::kBytes);
+  if (e != cudaSuccess) return e;
   *grid = sms * (per_sm > 0 ? per_sm : 1);
   if (dev >= 0 && dev < 64) grid_of_device[dev] = *grid;
   return cudaSuccess;
@@ -755,7 +704,8 @@ static cudaError_t launch_plan_and_stage1(const uint16_t* query, int64_t q_ss, i
                                           int max_blocks, int S, const Workspace& ws, unsigned* err,
                                           cudaStream_t stream, cudaEvent_t ev_before,
                                           cudaEvent_t ev_after) {
-  using Lay = Stage1Layout<NT>;
+  constexpr int NWARPS = 4, NSTAGE = kStage1Stages;
+  using Lay = Stage1Layout<NT, NWARPS, NSTAGE>;
   int grid = 0;
   cudaError_t e = stage1_grid<NT>(&grid);
   if (e != cudaSuccess) return e;
@@ -764,7 +714,7 @@ static cudaError_t launch_plan_and_stage1(const uint16_t* query, int64_t q_ss, i
   decode_plan<<<1, kPlanThreads, 0, stream>>>(sl, B, Hk, S, max_blocks, grid * kUnitsPerCta, ws);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (ev_before && (e = record_timing_event(ev_before, stream)) != cudaSuccess) return e;
-  decode_stage1<NT><<<grid, kS1Warps * 32, Lay::kBytes, stream>>>(
+  decode_stage1<NT, NWARPS, NSTAGE><<<grid, NWARPS * 32, Lay::kBytes, stream>>>(
       query, q_ss, q_sh, kv_map, bt, sl, scale * kLog2e, Hq, Hk, Hq / Hk, num_blocks, max_blocks, S,
       ws, err);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -21,6 +21,9 @@ constexpr int kTileBytes = kPage * kSlotBytes;   // 4352 bytes per (page, kv hea
 #ifndef UQ_S1_NSTAGE
 #define UQ_S1_NSTAGE 2
 #endif
+#ifndef UQ_S1_MIN_BLOCKS
+#define UQ_S1_MIN_BLOCKS 4
+#endif
 constexpr int kMinPagesPerUnit = UQ_MIN_PAGES_PER_UNIT;  // floor of 128 tokens per split
 constexpr int kUnitsPerCta = UQ_UNITS_PER_CTA;           // work units per resident CTA
 constexpr int kStage1Stages = UQ_S1_NSTAGE;              // pages in flight per warp
@@ -71,6 +74,12 @@ __device__ __forceinline__ int clamp_len(int L, int max_blocks) {
   L = max(L, 0);
   const long long cap = (long long)max_blocks * kPage;
   return (long long)L > cap ? (int)cap : L;
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                            uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
 }
 
 }  // namespace uq

@@ -61,16 +61,6 @@ __device__ __forceinline__ void f16x2x4_from_e2m1_word(uint32_t w, uint32_t (&o)
       : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3]) : "r"(w));
 }
 
-// Four fp32 -> four E4M3 bytes (round to nearest even, saturating at
-// +-448), `a` in the lowest byte.
-__device__ __forceinline__ uint32_t e4m3x4_from_f32(float a, float b, float c, float d) {
-  uint32_t r;
-  asm("{\n\t.reg .b16 lo, hi;\n\tcvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
-      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\tmov.b32 %0, {lo, hi};\n}\n"
-      : "=r"(r) : "f"(a), "f"(b), "f"(c), "f"(d));
-  return r;
-}
-
 // Two fp32 -> E4M3 (round to nearest even, saturating at +-448) -> f16x2
 // holding those E4M3 values exactly; `lo` lands in the low half.
 __device__ __forceinline__ uint32_t e4m3_roundtrip_f16x2(float lo, float hi) {
@@ -237,10 +227,6 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
                :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
-__device__ __forceinline__ void sts64(uint32_t addr, uint32_t a, uint32_t b) {
-  asm volatile("st.shared.v2.u32 [%0], {%1,%2};" :: "r"(addr), "r"(a), "r"(b) : "memory");
-}
-
 __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   uint2 v;
   asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
@@ -252,93 +238,6 @@ __device__ __forceinline__ uint4 ldg_nc_128(const void* p) {
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
   return v;
-}
-
-// ---------------------------------------------------------------------------
-// Tensor memory and the 5th-generation tensor cores (tcgen05), one CTA.
-// A tensor-memory address holds the lane in bits 31..16 and the column in
-// bits 15..0; warp w of a CTA reaches lanes 32 (w % 4) .. 32 (w % 4) + 31.
-// ---------------------------------------------------------------------------
-// One full warp allocates `ncols` columns (a power of two >= 32) and writes
-// the base address to shared memory at `dst_smem`.
-__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-               :: "r"(dst_smem), "r"(ncols) : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols) : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before_sync() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void tc_fence_after_sync() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// 16 lanes x 256 bits from registers: thread (g = lane/4, c = lane%4) writes
-// lane g columns 2c, 2c+1 (a, b) and lane g+8 columns 2c, 2c+1 (c2, d).
-__device__ __forceinline__ void tmem_st_16x256b(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c2,
-                                                uint32_t d) {
-  asm volatile("tcgen05.st.sync.aligned.16x256b.x1.b32 [%0], {%1,%2,%3,%4};"
-               :: "r"(taddr), "r"(a), "r"(b), "r"(c2), "r"(d) : "memory");
-}
-
-__device__ __forceinline__ void tmem_wait_st() {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-// 16 lanes x 8 fp32 columns into the mma.m16n8 accumulator layout: thread
-// (g, c) gets (lane g, col 2c), (g, 2c+1), (g+8, 2c), (g+8, 2c+1).  The wait
-// sits in the same statement, so the registers are valid on return.
-__device__ __forceinline__ void tmem_ld_16x256b_x1(uint32_t taddr, float (&v)[4]) {
-  uint32_t r0, r1, r2, r3;
-  asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];\n\t"
-               "tcgen05.wait::ld.sync.aligned;"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(taddr) : "memory");
-  v[0] = __uint_as_float(r0); v[1] = __uint_as_float(r1);
-  v[2] = __uint_as_float(r2); v[3] = __uint_as_float(r3);
-}
-
-// As above for 16 columns: v[0..3] columns 0..7, v[4..7] columns 8..15.
-__device__ __forceinline__ void tmem_ld_16x256b_x2(uint32_t taddr, float (&v)[8]) {
-  uint32_t r[8];
-  asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t"
-               "tcgen05.wait::ld.sync.aligned;"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-                 "=r"(r[6]), "=r"(r[7])
-               : "r"(taddr) : "memory");
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// Shared-memory matrix descriptor, no swizzle: the operand is stored as 8-row
-// x 16-byte core matrices; `lbo` is the byte distance between core matrices
-// along K, `sbo` between 8-row groups along M (or N).
-__device__ __forceinline__ uint64_t smem_desc_noswizzle(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((saddr >> 4) & 0x3FFFu) | (uint64_t)((lbo >> 4) & 0x3FFFu) << 16 |
-         (uint64_t)((sbo >> 4) & 0x3FFFu) << 32 | (uint64_t)1 << 46;
-}
-
-// D (+)= (A x 2^sfa) (B x 2^sfb)^T with UE8M0 block scales, one 32-element
-// block of K per instruction (kind::mxf8f6f4, scale_vec 1X).
-__device__ __forceinline__ void tc_mma_block_scaled(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                                    uint32_t idesc, uint32_t sfa_tmem,
-                                                    uint32_t sfb_tmem, uint32_t accumulate) {
-  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-               "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n\t}\n"
-               :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
-                  "r"(accumulate) : "memory");
-}
-
-// Arrive once on `bar` when every tcgen05 operation this thread issued so
-// far has completed.
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-               :: "r"(bar) : "memory");
 }
 
 }  // namespace uq
