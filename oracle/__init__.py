@@ -56,6 +56,8 @@ def lib() -> ctypes.CDLL:
                                 c_int, c_int, c_p]
         L.uqo_store_f32.restype = c_i64
         L.uqo_store_f32.argtypes = [c_p, c_p, c_p, c_i64, c_int, c_int, c_int, c_int, c_p]
+        L.uqo_full_dequant.restype = c_int
+        L.uqo_full_dequant.argtypes = [c_p, c_p, c_int, c_int, c_int, c_int, c_int, c_p, c_p]
         L.uqo_query_prime.restype = None
         L.uqo_query_prime.argtypes = [c_p, c_int, c_p, c_p]
         L.uqo_decode.restype = c_int
@@ -177,6 +179,25 @@ def store_f32(k_rot: np.ndarray, v: np.ndarray, slot_mapping: np.ndarray,
     nb, bs, _, _ = kv_cache.shape
     return lib().uqo_store_f32(_ptr(k_rot), _ptr(v), _ptr(sm), N, Hk, D, nb, bs,
                                _ptr(kv_cache))
+
+
+def full_dequant(kv_cache: np.ndarray, block_table: np.ndarray, n_pages: int | None = None):
+    """Dequantise one sequence's pages into bf16 bit patterns.
+
+    kv_cache: uint8 [num_blocks, block_size, Hk, slot]; block_table: int32
+    page ids of the sequence.  Returns (k_bits, v_bits, n_bad_pages) with
+    k_bits, v_bits uint16 [Hk, n_pages * block_size, D] (K still rotated).
+    """
+    bt = np.ascontiguousarray(block_table, dtype=np.int32).reshape(-1)
+    n = int(bt.shape[0]) if n_pages is None else int(n_pages)
+    kv_cache = np.ascontiguousarray(kv_cache, dtype=np.uint8)
+    nb, bs, Hk, sbytes = kv_cache.shape
+    D = (sbytes // 17) * 16
+    assert sbytes == slot_bytes(D)
+    k = np.zeros((Hk, n * bs, D), dtype=np.uint16)
+    v = np.zeros((Hk, n * bs, D), dtype=np.uint16)
+    bad = lib().uqo_full_dequant(_ptr(kv_cache), _ptr(bt), n, Hk, D, nb, bs, _ptr(k), _ptr(v))
+    return k, v, int(bad)
 
 
 def query_prime(q_bits: np.ndarray) -> np.ndarray:

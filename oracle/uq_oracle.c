@@ -32,6 +32,9 @@
  *   uqo_decode          pinned: L=1, equal keys, dominant logit, head map,
  *                       page permutation invariance, numpy brute force
  *   uqo_decode (S > 0)  pinned: equals the single softmax to 1e-12
+ *   uqo_full_dequant    pinned: numpy bit-level mirror on tiny caches, spike
+ *                       slot, closed forms at scale bytes 0, 254 and 255,
+ *                       page-permutation invariance
  */
 #include <math.h>
 #include <stdint.h>
@@ -316,6 +319,54 @@ int64_t uqo_store_f32(const float *k_rot, const float *v,
                               kv_cache + slot_offset(slot, h, Hk, block_size, sb));
     }
     return skipped;
+}
+
+/*
+ * [ultraquant_attn: _ultraquant_continuation_prefill, the call to
+ * ultraquant_full_dequant_kv] dequantise the cached prefix of one sequence
+ * into bf16 buffers shaped (1, Hk, alloc_len, D), alloc_len = n_pages *
+ * block_size (whole pages).  K stays Hadamard-rotated, as stored; V is in
+ * the original space.  Token t of page p is slot block_table[p] * block_size
+ * + t.  Each value is LUT[code] * 2^(byte - 127) in fp64 (a scale byte of 255
+ * is read as 2^128 by the same formula; the store never writes it), then
+ * bf16 round-to-nearest-even (inf on overflow).  Reading: a page id outside
+ * [0, num_blocks) leaves its rows zero.  Returns the number of such pages.
+ */
+int uqo_full_dequant(const uint8_t *kv_cache, const int32_t *block_table, int n_pages,
+                     int Hk, int D, int num_blocks, int block_size,
+                     uint16_t *k_out, uint16_t *v_out)
+{
+    int sb = uqo_slot_bytes(D);
+    int64_t alloc_len = (int64_t)n_pages * block_size;
+    double *k = (double *)malloc(sizeof(double) * D);
+    double *v = (double *)malloc(sizeof(double) * D);
+    int bad = 0;
+    for (int p = 0; p < n_pages; ++p) {
+        int32_t pid = block_table[p];
+        int ok = pid >= 0 && pid < num_blocks;
+        if (!ok) ++bad;
+        for (int t = 0; t < block_size; ++t) {
+            int64_t slot = (int64_t)pid * block_size + t;
+            int64_t row = (int64_t)p * block_size + t;
+            for (int h = 0; h < Hk; ++h) {
+                uint16_t *ko = k_out + ((int64_t)h * alloc_len + row) * D;
+                uint16_t *vo = v_out + ((int64_t)h * alloc_len + row) * D;
+                if (!ok) {
+                    memset(ko, 0, sizeof(uint16_t) * D);
+                    memset(vo, 0, sizeof(uint16_t) * D);
+                    continue;
+                }
+                uqo_dequant_slot(kv_cache + slot_offset(slot, h, Hk, block_size, sb), D, k, v);
+                for (int d = 0; d < D; ++d) {
+                    ko[d] = uqo_bf16_round(k[d]);
+                    vo[d] = uqo_bf16_round(v[d]);
+                }
+            }
+        }
+    }
+    free(k);
+    free(v);
+    return bad;
 }
 
 /* ------------------------------------------------------------------------- */
