@@ -55,18 +55,22 @@ def _peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def _source_hash() -> str:
+DEQUANT_SOURCES = ["bit_quantized_kv_gb300/csrc/uq_dequant.cu", "bit_quantized_kv_gb300/csrc/uq_device.cuh"]
+
+
+def _source_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in (KERNEL_SOURCES if sources is None else sources):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def _traffic_from_profile(workload: str):
-    """DRAM bytes per stage-1 launch from the committed ncu summary, if it was
-    taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", f"decode_stage1_{workload}.md")
+def _traffic_from_profile(workload: str, profile: str | None = None, sources=None):
+    """DRAM bytes per launch of the workload's dominant kernel from the
+    committed ncu summary, if it was taken on the current kernel source; else
+    None."""
+    path = os.path.join(ROOT, "profiles", profile or f"decode_stage1_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
@@ -76,7 +80,7 @@ def _traffic_from_profile(workload: str):
         if ":" in line and line.strip().startswith("- "):
             k, _, v = line.strip()[2:].partition(":")
             vals[k.strip()] = v.strip().strip("`")
-    if vals.get("source_sha256_16") != _source_hash():
+    if vals.get("source_sha256_16") != _source_hash(sources):
         return None
     try:
         return float(vals["dram_bytes_per_launch_full_size"])
@@ -235,6 +239,8 @@ def run_gpu(args, rank, local, world):
 
     if args.workload == "store":
         return run_gpu_store(args, rank, local, world, dev, stream, peak, peak_kind)
+    if args.workload == "dequant":
+        return run_gpu_dequant(args, rank, local, world, dev, stream, peak, peak_kind)
 
     wl = rank_workload(args.workload, rank, world)
     with torch.cuda.stream(stream):
@@ -410,6 +416,82 @@ def run_gpu_store(args, rank, local, world, dev, stream, peak, peak_kind):
             "gpu_launches": args.steps, "clocks": clocks.summary()}
 
 
+def run_gpu_dequant(args, rank, local, world, dev, stream, peak, peak_kind):
+    """Full-prefix dequantisation of one 32768-token sequence (8 kv heads):
+    each step expands its 2048 pages to bf16 K and V (340 MB moved per step,
+    above L2)."""
+    import torch
+    from bit_quantized_kv_gb300 import binding, workloads
+    wl = workloads.dequant_workload("dequant")
+    n = wl.block_table.shape[1]
+    with torch.cuda.stream(stream):
+        cache = torch.zeros((wl.num_blocks, wl.block_size, wl.Hk, 272), dtype=torch.uint8, device=dev)
+        k, v = workloads.sequence_kv(wl, 0, dev)
+        binding.uq_store(k, v, cache, torch.from_numpy(workloads.sequence_slots(wl, 0)).to(dev))
+        bt = torch.from_numpy(np.ascontiguousarray(wl.block_table[0])).to(dev)
+        k_out = torch.empty((wl.Hk, n * wl.block_size, wl.D), dtype=torch.bfloat16, device=dev)
+        v_out = torch.empty_like(k_out)
+        for _ in range(args.warmup):
+            binding.uq_full_dequant(cache, bt, k_out, v_out)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        _barrier(world)
+        with ClockSampler(local) as clocks:
+            for a, b in evs:
+                a.record(stream)
+                binding.uq_full_dequant(cache, bt, k_out, v_out)
+                b.record(stream)
+            torch.cuda.synchronize()
+        ms = [a.elapsed_time(b) for a, b in evs]
+    total = _max_over_ranks(sum(ms), world)
+    ms_step = total / args.steps
+    by = workloads.dequant_bytes(wl)
+    ach = by / (statistics.mean(ms) * 1e-3) / 1e9
+    line = {"metric": METRIC, "value": round(world * by / (ms_step * 1e-3) / 1e9, 2), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp4-e2m1 cache in, bf16 out", "data": "synthetic",
+            "config": {"workload": "dequant", "seq_len": int(wl.seq_lens[0]), "pages": n,
+                       "Hk": wl.Hk, "D": wl.D, "bytes_per_step": by,
+                       "l2": "inputs and outputs larger than L2 (340 MB per step)"},
+            "roofline": {"bound": "hbm", "kernel": "full_dequant", "achieved": round(ach, 2),
+                         "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
+                         "frac": round(ach / peak, 4),
+                         "traffic": _traffic_from_profile("dequant", "full_dequant_dequant.md", DEQUANT_SOURCES)},
+            "gpu_launches": args.steps, "clocks": clocks.summary()}
+    if rank == 0 and not args.no_cpu_baseline:
+        nbytes, secs, desc = _oracle_dequant_sample(wl, args.cpu_budget)
+        line["cpu_baseline"] = {"value": round(nbytes / secs / 1e9, 6), "unit": UNIT, "cores": 1,
+                                "kind": "oracle", "sample": desc}
+    return line
+
+
+def _oracle_dequant_sample(wl, budget_s: float):
+    """Time the oracle's full dequantisation over pages of its own packing of
+    the dequant workload, one call per 64 pages, until about budget_s seconds;
+    return (bytes, seconds, description)."""
+    import torch
+    import oracle
+    from bit_quantized_kv_gb300 import workloads
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    k, v = workloads.sequence_kv(wl, 0, dev)
+    kb = k.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    vb = v.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    L = int(wl.seq_lens[0])
+    P = (L + 15) // 16
+    cache = np.zeros((P, 16, wl.Hk, 272), np.uint8)
+    oracle.store(kb, vb, np.arange(L, dtype=np.int64), cache)          # untimed set-up
+    spent, pages = 0.0, 0
+    while spent < budget_s and pages < P:
+        chunk = np.arange(pages, min(P, pages + 64), dtype=np.int32)
+        t0 = time.perf_counter()
+        oracle.full_dequant(cache, chunk)
+        spent += time.perf_counter() - t0
+        pages += len(chunk)
+    nbytes = pages * 16 * wl.Hk * (272 + 1024) + 4 * pages
+    return nbytes, spent, f"{pages} of {P} pages of workload dequant (1 thread); oracle packing untimed"
+
+
 # --------------------------------------------------------------------------- #
 # CPU oracle (baseline / reference arm)                                        #
 # --------------------------------------------------------------------------- #
@@ -462,6 +544,8 @@ def run_reference(args, rank, world):
     from bit_quantized_kv_gb300 import workloads
     if rank != 0:
         return None
+    if args.workload == "dequant":
+        return run_reference_dequant(args, world)
     wl = workloads.decode_workload(args.workload) if args.workload != "store" else None
     if wl is None:
         return {"impl": "reference", "unavailable": "store workload has no oracle timing arm"}
@@ -486,13 +570,38 @@ def run_reference(args, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
+def run_reference_dequant(args, world):
+    from bit_quantized_kv_gb300 import workloads
+    wl = workloads.dequant_workload("dequant")
+    per_step = max(1.0, args.cpu_budget / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        _oracle_dequant_sample(wl, per_step)
+    tot_b, tot_s, desc = 0, 0.0, ""
+    for _ in range(args.steps):
+        b, sec, desc = _oracle_dequant_sample(wl, per_step)
+        tot_b += b
+        tot_s += sec
+    val = tot_b / tot_s / 1e9
+    return {"metric": METRIC, "value": round(val, 6), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * tot_s / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": "dequant", "seq_len": int(wl.seq_lens[0]), "Hk": wl.Hk, "D": wl.D},
+            "cpu_baseline": {"value": round(val, 6), "unit": UNIT, "cores": 1,
+                             "kind": "oracle", "sample": "each step: " + desc},
+            "e2e": {"value": round(val, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="outlier_long",
-                    choices=["tiny", "batch", "outlier_long", "skewed", "outlier_ncu", "store"])
+                    choices=["tiny", "batch", "outlier_long", "skewed", "outlier_ncu", "store",
+                             "dequant"])
     ap.add_argument("--impl", default="uq", choices=["uq", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the CPU baseline")

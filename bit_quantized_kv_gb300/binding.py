@@ -32,7 +32,7 @@ HEAD_DIM = 256
 SLOT_BYTES = 272
 
 EXPORTED = ("uq_version", "uq_slot_bytes", "uq_decode_workspace_bytes", "uq_store",
-            "uq_store_rotated_f32", "uq_decode", "uq_decode_static_scratch",
+            "uq_store_rotated_f32", "uq_decode", "uq_full_dequant", "uq_decode_static_scratch",
             "uq_set_timing_events", "uq_last_error", "uq_check_device_error")
 
 
@@ -70,6 +70,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.uq_decode.restype = c_int
     L.uq_decode.argtypes = [c_p, c_p, c_p, c_p, c_f, c_int, c_p, c_sz, c_p, c_int, c_int,
                             c_int, c_int, c_int, c_int, c_int, c_int, c_i64, c_i64, c_p]
+    L.uq_full_dequant.restype = c_int
+    L.uq_full_dequant.argtypes = [c_p, c_p, c_int, c_p, c_p, c_int, c_int, c_int, c_int, c_int, c_p]
     L.uq_decode_static_scratch.restype = c_int
     L.uq_decode_static_scratch.argtypes = [c_p, c_p, c_p, c_p, c_f, c_int, c_p, c_int, c_int,
                                            c_int, c_int, c_int, c_int, c_int, c_int, c_i64,
@@ -194,6 +196,29 @@ def uq_decode(query: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Te
                             nb, bs, block_table.shape[1], sb, query.stride(0), query.stride(1),
                             _stream_ptr(stream)))
     return out
+
+
+def uq_full_dequant(kv_cache: torch.Tensor, block_table: torch.Tensor, k_out: torch.Tensor,
+                    v_out: torch.Tensor, n_pages: int | None = None, stream=None):
+    """Expand one sequence's pages to bf16: kv_cache uint8 [num_blocks, 16,
+    Hk, 272]; block_table int32 [>= n_pages] page ids; k_out, v_out bf16
+    [Hk, n_pages * 16, 256] contiguous (K stays rotated).  Returns (k_out, v_out)."""
+    _need(kv_cache, "kv_cache", torch.uint8, 4)
+    _need(block_table, "block_table", torch.int32, 1)
+    _need(k_out, "k_out", torch.bfloat16, 3)
+    _need(v_out, "v_out", torch.bfloat16, 3)
+    n = block_table.shape[0] if n_pages is None else int(n_pages)
+    nb, bs, Hk, sb = kv_cache.shape
+    if n > block_table.shape[0]:
+        raise ValueError("block_table has fewer entries than n_pages")
+    for t in (k_out, v_out):
+        if tuple(t.shape) != (Hk, n * bs, HEAD_DIM) or not t.is_contiguous():
+            raise ValueError(f"k_out / v_out must be contiguous [{Hk}, {n * bs}, {HEAD_DIM}]")
+    if not (kv_cache.is_contiguous() and block_table.is_contiguous()):
+        raise ValueError("kv_cache and block_table must be contiguous")
+    _check(load().uq_full_dequant(kv_cache.data_ptr(), block_table.data_ptr(), n, k_out.data_ptr(),
+                                  v_out.data_ptr(), Hk, HEAD_DIM, nb, bs, sb, _stream_ptr(stream)))
+    return k_out, v_out
 
 
 def uq_decode_static_scratch(query: torch.Tensor, kv_cache: torch.Tensor,

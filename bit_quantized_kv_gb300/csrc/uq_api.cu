@@ -24,6 +24,9 @@ cudaError_t launch_decode(const uint16_t* query, int64_t q_ss, int64_t q_sh, con
                           uint16_t* out, unsigned* err, cudaStream_t stream,
                           cudaEvent_t ev_before_stage1, cudaEvent_t ev_after_stage1);
 size_t decode_workspace_bytes(int B, int Hq, int S);
+cudaError_t launch_full_dequant(const uint8_t* kv, const int32_t* block_table, int n_pages, int Hk,
+                                int num_blocks, uint16_t* k_out, uint16_t* v_out, unsigned* err,
+                                cudaStream_t stream);
 }  // namespace uq
 
 namespace {
@@ -159,6 +162,33 @@ uq_status uq_store_rotated_f32(const float* key_rot, const float* value, void* k
                                    num_kv_heads, 0, 0, block_size, (int64_t)num_blocks * block_size,
                                    err, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(UQ_ERR_CUDA, "store launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+uq_status uq_full_dequant(const void* kv_cache, const int32_t* block_table, int n_pages,
+                          void* k_out, void* v_out, int Hk, int head_dim, int num_blocks,
+                          int block_size, int slot_bytes, void* stream) {
+  if (head_dim != uq::kHeadDim) return fail(UQ_ERR_UNSUPPORTED, "head_dim %d unsupported (only 256)", head_dim);
+  if (block_size != 16) return fail(UQ_ERR_UNSUPPORTED, "block_size %d unsupported (only 16)", block_size);
+  if (slot_bytes != uq::kSlotBytes) return fail(UQ_ERR_INVALID_ARG, "slot_bytes %d != 272", slot_bytes);
+  if (Hk < 1 || Hk > 256) return fail(UQ_ERR_UNSUPPORTED, "Hk %d outside [1, 256]", Hk);
+  if (num_blocks < 1) return fail(UQ_ERR_INVALID_ARG, "num_blocks %d < 1", num_blocks);
+  if (n_pages < 0 || (int64_t)n_pages * block_size >= ((int64_t)1 << 31) ||
+      (int64_t)n_pages * Hk >= ((int64_t)1 << 31))
+    return fail(UQ_ERR_INVALID_ARG, "n_pages %d: need n_pages * block_size and n_pages * Hk < 2^31", n_pages);
+  if (n_pages == 0) return ok();
+  if (!kv_cache || !block_table || !k_out || !v_out)
+    return fail(UQ_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(kv_cache, 16) || !aligned(k_out, 16) || !aligned(v_out, 16) || !aligned(block_table, 4))
+    return fail(UQ_ERR_INVALID_ARG, "kv_cache, k_out, v_out must be 16-byte aligned, block_table 4-byte");
+  unsigned int* err = nullptr;
+  uq_status st = error_word(&err);
+  if (st != UQ_OK) return st;
+  cudaError_t e = uq::launch_full_dequant(static_cast<const uint8_t*>(kv_cache), block_table, n_pages,
+                                          Hk, num_blocks, static_cast<uint16_t*>(k_out),
+                                          static_cast<uint16_t*>(v_out), err,
+                                          static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(UQ_ERR_CUDA, "full dequant launch: %s", cudaGetErrorString(e));
   return ok();
 }
 

@@ -16,6 +16,9 @@ synthetic draws stand in for real traffic):
     (``seed * 1_000_003 + b + 1``) so one sequence can be regenerated alone.
   * outlier-K workload: 4 channels per kv head drawn once from the seed,
     multiplied by 20 in every token of K.
+  * full-dequant workload: one sequence of 32768 tokens (2048 pages) and 8 kv
+    heads, its K/V drawn like a decode workload's and written with uq_store;
+    pages are a random permutation of the cache.
   * store workload: K and V ~ N(0, 1) with independent Bernoulli(0.01)
     masks multiplying entries by 50; slots are the first N of a random
     permutation of all num_blocks * block_size slots.
@@ -228,3 +231,26 @@ def store_inputs(wl: StoreWorkload, device="cpu"):
     rng = np.random.default_rng(wl.seed)
     slots = rng.permutation(wl.num_blocks * wl.block_size)[:wl.N].astype(np.int64)
     return k, v, torch.from_numpy(slots).to(device)
+
+
+def dequant_workload(name: str = "dequant") -> DecodeWorkload:
+    """One long sequence whose cached prefix is expanded to bf16.
+
+    dequant        L=32768 (2048 pages), Hk=8 (Hq=64, unused by the kernel), seed 6
+    dequant_small  L=1000 (63 pages, ragged last page), Hk=3, seed 7
+    """
+    if name == "dequant":
+        return make_decode_workload("dequant", 1, 64, 8, np.array([32768]), 32768 // BLOCK_SIZE, 1,
+                                    seed=6, spare_blocks=5)
+    if name == "dequant_small":
+        return make_decode_workload("dequant_small", 1, 18, 3, np.array([1000]), 64, 1, seed=7,
+                                    spare_blocks=2)
+    raise KeyError(name)
+
+
+def dequant_bytes(wl: DecodeWorkload) -> int:
+    """Bytes one full dequantisation moves: whole pages read (272 B per
+    (token, kv head)), bf16 K and V written (1024 B), page ids read."""
+    pages = int((int(wl.seq_lens[0]) + wl.block_size - 1) // wl.block_size)
+    rows = pages * wl.block_size * wl.Hk
+    return rows * (wl.D + wl.D // 16) + rows * wl.D * 2 * 2 + pages * 4

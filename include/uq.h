@@ -172,6 +172,33 @@ uq_status uq_decode(const void *query, const void *kv_cache,
                     int64_t q_stride_head, void *stream);
 
 /*
+ * uq_full_dequant -- expand one sequence's cached prefix to bf16
+ * (ultraquant_attn, UltraQuantAttentionImpl._ultraquant_continuation_prefill:
+ * the call to ultraquant_full_dequant_kv that feeds a large continuation
+ * chunk's dense prefill).
+ *
+ *   kv_cache     uint8 cache written by uq_store (read only).
+ *   block_table  int32 [n_pages]: the sequence's page ids, in order.
+ *   n_pages      pages to expand (>= 0): alloc_len = n_pages * block_size
+ *                rows, ceil(cached_len / block_size) pages for a prefix of
+ *                cached_len tokens.
+ *   k_out, v_out bf16 [Hk][alloc_len][D] contiguous (the pages' buffer
+ *                (1, Hk, alloc_len, D) without the leading 1), written;
+ *                16-byte aligned.  Row t of page p is row p * block_size + t.
+ *
+ * K stays Hadamard-rotated, as stored; V is in the original space.  Every
+ * element is E2M1(code) * 2^(byte - 127) rounded to bf16 (exact: at most two
+ * significant bits; a product beyond bf16's range becomes +-inf, which the
+ * store never produces).  A page id outside [0, num_blocks) writes zero rows
+ * and sets UQ_DEVERR_BAD_PAGE.  n_pages == 0 is a no-op.  Supported:
+ * head_dim 256, block_size 16, 1 <= Hk <= 256, n_pages * block_size < 2^31
+ * and n_pages * Hk < 2^31.
+ */
+uq_status uq_full_dequant(const void *kv_cache, const int32_t *block_table, int n_pages,
+                          void *k_out, void *v_out, int Hk, int head_dim, int num_blocks,
+                          int block_size, int slot_bytes, void *stream);
+
+/*
  * uq_decode_static_scratch -- uq_decode for callers that cannot allocate
  * device memory.  The paper has no counterpart; this entry point exists for
  * integrations where nobody can hand uq_decode a workspace: for example a

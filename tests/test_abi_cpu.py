@@ -132,6 +132,37 @@ def test_store_rotated_rejects_invalid_arguments(lib):
     assert st == binding.UQ_ERR_INVALID_ARG
 
 
+def _dequant(lib, **kw):
+    args = dict(kv=FAKE, bt=FAKE, n=3, k=FAKE, v=FAKE, Hk=2, D=256, nb=4, bs=16, sb=272)
+    args.update(kw)
+    return lib.uq_full_dequant(args["kv"], args["bt"], args["n"], args["k"], args["v"], args["Hk"],
+                               args["D"], args["nb"], args["bs"], args["sb"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=128), binding.UQ_ERR_UNSUPPORTED),
+    (dict(bs=32), binding.UQ_ERR_UNSUPPORTED),
+    (dict(Hk=0), binding.UQ_ERR_UNSUPPORTED),
+    (dict(Hk=300), binding.UQ_ERR_UNSUPPORTED),
+    (dict(sb=288), binding.UQ_ERR_INVALID_ARG),
+    (dict(nb=0), binding.UQ_ERR_INVALID_ARG),
+    (dict(n=-1), binding.UQ_ERR_INVALID_ARG),
+    (dict(n=1 << 27), binding.UQ_ERR_INVALID_ARG),         # n * 16 >= 2^31
+    (dict(n=1 << 24, Hk=256), binding.UQ_ERR_INVALID_ARG), # n * Hk >= 2^31
+    (dict(kv=0), binding.UQ_ERR_INVALID_ARG),
+    (dict(k=0), binding.UQ_ERR_INVALID_ARG),
+    (dict(k=FAKE + 8), binding.UQ_ERR_INVALID_ARG),        # misaligned
+    (dict(bt=FAKE + 2), binding.UQ_ERR_INVALID_ARG),
+])
+def test_full_dequant_rejects_invalid_arguments(lib, kw, status):
+    assert _dequant(lib, **kw) == status
+    assert lib.uq_last_error().decode() != ""
+
+
+def test_full_dequant_zero_pages_is_a_noop(lib):
+    assert _dequant(lib, n=0, kv=0, bt=0, k=0, v=0) == binding.UQ_OK
+
+
 def test_python_binding_rejects_cpu_tensors(lib):
     import torch
     q = torch.zeros(1, 8, 256, dtype=torch.bfloat16)
