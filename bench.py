@@ -241,6 +241,8 @@ def run_gpu(args, rank, local, world):
         return run_gpu_store(args, rank, local, world, dev, stream, peak, peak_kind)
     if args.workload == "dequant":
         return run_gpu_dequant(args, rank, local, world, dev, stream, peak, peak_kind)
+    if args.workload == "mq":
+        return run_gpu_mq(args, rank, local, world, dev, stream, peak, peak_kind)
 
     wl = rank_workload(args.workload, rank, world)
     with torch.cuda.stream(stream):
@@ -466,6 +468,106 @@ def run_gpu_dequant(args, rank, local, world, dev, stream, peak, peak_kind):
     return line
 
 
+def run_gpu_mq(args, rank, local, world, dev, stream, peak, peak_kind):
+    """Multi-query continuation decode: 8 draft tokens after 131072 cached
+    tokens of one sequence (GQA 8).  GB/s counts each cached byte once (the
+    8 rows share the pages; repeats come from L2)."""
+    import torch
+    from bit_quantized_kv_gb300 import binding, workloads
+    wl, cached, q_len = workloads.multi_query_workload("mq")
+    S = wl.splits
+    with torch.cuda.stream(stream):
+        cache = torch.zeros((wl.num_blocks, wl.block_size, wl.Hk, 272), dtype=torch.uint8, device=dev)
+        k, v = workloads.sequence_kv(wl, 0, dev)
+        binding.uq_store(k, v, cache, torch.from_numpy(workloads.sequence_slots(wl, 0)).to(dev))
+        q = workloads.chunk_query(wl, q_len, dev)
+        bt = torch.from_numpy(np.ascontiguousarray(wl.block_table[0])).to(dev)
+        ws = torch.empty(binding.uq_decode_workspace_bytes(q_len, wl.Hq, wl.D, S), dtype=torch.uint8, device=dev)
+        out = torch.empty_like(q)
+        for _ in range(args.warmup):
+            binding.uq_decode_multi_query(q, cache, bt, cached, wl.scale, S, ws, out)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        s1 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for a, b in s1:
+            a.record(stream)
+            b.record(stream)
+        torch.cuda.synchronize()
+        _barrier(world)
+        with ClockSampler(local) as clocks:
+            for (a, b), (c, d) in zip(evs, s1):
+                binding.uq_set_timing_events(c, d)
+                a.record(stream)
+                binding.uq_decode_multi_query(q, cache, bt, cached, wl.scale, S, ws, out)
+                b.record(stream)
+            torch.cuda.synchronize()
+        binding.uq_set_timing_events(None, None)
+        ms = [a.elapsed_time(b) for a, b in evs]
+        ms1 = [c.elapsed_time(d) for c, d in s1]
+    total = _max_over_ranks(sum(ms), world)
+    ms_step = total / args.steps
+    kv_bytes = (cached + q_len) * wl.Hk * 272
+    by = kv_bytes + 2 * q_len * wl.Hq * wl.D * 2
+    ach = by / (statistics.mean(ms1) * 1e-3) / 1e9
+    return {"metric": METRIC, "value": round(world * by / (ms_step * 1e-3) / 1e9, 2), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp4-e2m1 cache, f16 mma, f32 accumulate", "data": "synthetic",
+            "decode_tokens_per_s": round(world * q_len / (ms_step * 1e-3), 1),
+            "config": {"workload": "mq", "cached_len": cached, "q_len": q_len, "Hq": wl.Hq, "Hk": wl.Hk,
+                       "D": wl.D, "max_num_kv_splits": S, "bytes_per_step": by,
+                       "l2": "cache larger than L2 (285 MB per step)"},
+            "roofline": {"bound": "hbm", "kernel": "decode_stage1", "achieved": round(ach, 2),
+                         "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
+                         "frac": round(ach / peak, 4), "traffic": None,
+                         "stage1_ms": round(statistics.mean(ms1), 5)},
+            "gpu_launches": args.steps * 3, "clocks": clocks.summary(),
+            **({} if (rank != 0 or args.no_cpu_baseline) else {"cpu_baseline": _mq_cpu_baseline(args.cpu_budget)})}
+
+
+def _oracle_mq_sample(budget_s: float):
+    """Time the oracle's decode of the mq workload's synthetic batch, one
+    (chunk row, query head) at a time over the host cores, until about
+    budget_s seconds; return (bytes, seconds, threads, description).  Bytes
+    count the cached pages once per chunk row, as the GPU line does per step."""
+    import torch
+    import oracle
+    from bit_quantized_kv_gb300 import workloads
+    wl, cached, q_len = workloads.multi_query_workload("mq")
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    k, v = workloads.sequence_kv(wl, 0, dev)
+    kb = k.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    vb = v.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    L = cached + q_len
+    P = (L + 15) // 16
+    cache = np.zeros((P, 16, wl.Hk, 272), np.uint8)
+    oracle.store(kb, vb, np.arange(L, dtype=np.int64), cache)          # untimed set-up
+    q = workloads.chunk_query(wl, q_len, dev)
+    qb = q.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    table = np.tile(np.arange(P, dtype=np.int32), (q_len, 1))
+    lens = (cached + 1 + np.arange(q_len)).astype(np.int32)
+    threads = min(os.cpu_count() or 1, wl.Hq)
+    spent, rows_done = 0.0, 0
+    for i in range(q_len):
+        rows = np.array([[i, r] for r in range(wl.Hq)], np.int32)
+        t0 = time.perf_counter()
+        oracle.decode(qb, cache, table, lens, wl.scale, rows=rows, nthreads=threads)
+        spent += time.perf_counter() - t0
+        rows_done += 1
+        if spent >= budget_s:
+            break
+    nbytes = rows_done * ((cached + q_len) * wl.Hk * 272 / q_len + 2 * wl.Hq * wl.D * 2)
+    desc = (f"{rows_done} of {q_len} chunk rows (all {wl.Hq} query heads) of workload mq; "
+            f"oracle packing untimed")
+    return nbytes, spent, threads, desc
+
+
+def _mq_cpu_baseline(budget_s: float):
+    nbytes, secs, threads, desc = _oracle_mq_sample(budget_s)
+    return {"value": round(nbytes / secs / 1e9, 6), "unit": UNIT, "cores": threads,
+            "kind": "oracle", "sample": desc}
+
+
 def _oracle_dequant_sample(wl, budget_s: float):
     """Time the oracle's full dequantisation over pages of its own packing of
     the dequant workload, one call per 64 pages, until about budget_s seconds;
@@ -546,6 +648,24 @@ def run_reference(args, rank, world):
         return None
     if args.workload == "dequant":
         return run_reference_dequant(args, world)
+    if args.workload == "mq":
+        per_step = max(1.0, args.cpu_budget / max(1, args.steps + args.warmup))
+        tot_b, tot_s, desc, threads = 0.0, 0.0, "", 1
+        for it in range(args.warmup + args.steps):
+            b, sec, threads, desc = _oracle_mq_sample(per_step)
+            if it >= args.warmup:
+                tot_b += b
+                tot_s += sec
+        val = tot_b / tot_s / 1e9
+        return {"metric": METRIC, "value": round(val, 6), "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(1e3 * tot_s / args.steps, 3), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "impl": "reference", "config": {"workload": "mq"},
+                "cpu_baseline": {"value": round(val, 6), "unit": UNIT, "cores": threads,
+                                 "kind": "oracle", "sample": "each step: " + desc},
+                "e2e": {"value": round(val, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
     wl = workloads.decode_workload(args.workload) if args.workload != "store" else None
     if wl is None:
         return {"impl": "reference", "unavailable": "store workload has no oracle timing arm"}
@@ -601,7 +721,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="outlier_long",
                     choices=["tiny", "batch", "outlier_long", "skewed", "outlier_ncu", "store",
-                             "dequant"])
+                             "dequant", "mq"])
     ap.add_argument("--impl", default="uq", choices=["uq", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the CPU baseline")

@@ -11,7 +11,7 @@
 #include <cuda_runtime.h>
 
 #include "uq.h"
-#include "uq_device.cuh"
+#include "uq_decode_common.cuh"
 
 namespace uq {
 cudaError_t launch_store(bool rotated_f32, const void* key, const void* value, void* kv_cache,
@@ -19,7 +19,7 @@ cudaError_t launch_store(bool rotated_f32, const void* key, const void* value, v
                          int64_t key_stride, int64_t value_stride, int block_size,
                          int64_t num_slots, unsigned* err, cudaStream_t stream);
 cudaError_t launch_decode(const uint16_t* query, int64_t q_ss, int64_t q_sh, const uint8_t* kv,
-                          const int32_t* bt, const int32_t* sl, float scale, int B, int Hq,
+                          const int32_t* bt, const SeqRows& sl, float scale, int B, int Hq,
                           int Hk, int num_blocks, int max_blocks, int S, void* workspace,
                           uint16_t* out, unsigned* err, cudaStream_t stream,
                           cudaEvent_t ev_before_stage1, cudaEvent_t ev_after_stage1);
@@ -192,11 +192,17 @@ uq_status uq_full_dequant(const void* kv_cache, const int32_t* block_table, int 
   return ok();
 }
 
-uq_status uq_decode(const void* query, const void* kv_cache, const int32_t* block_table,
-                    const int32_t* seq_lens, float scale, int max_num_kv_splits, void* workspace,
-                    size_t workspace_bytes, void* out, int B, int Hq, int Hk, int head_dim,
-                    int num_blocks, int block_size, int max_blocks_per_seq, int slot_bytes,
-                    int64_t q_stride_seq, int64_t q_stride_head, void* stream) {
+namespace {
+
+// Checks shared by uq_decode and uq_decode_multi_query, in the order the
+// error messages report them.  *noop is set for an empty batch, which returns
+// UQ_OK before any pointer is looked at.
+uq_status check_decode(const void* query, const void* kv_cache, const int32_t* block_table,
+                       float scale, int max_num_kv_splits, const void* workspace,
+                       size_t workspace_bytes, const void* out, int B, int Hq, int Hk,
+                       int head_dim, int num_blocks, int block_size, int max_blocks_per_seq,
+                       int slot_bytes, int64_t q_stride_seq, int64_t q_stride_head, bool* noop) {
+  *noop = false;
   if (B < 0) return fail(UQ_ERR_INVALID_ARG, "B %d < 0", B);
   if (head_dim != uq::kHeadDim) return fail(UQ_ERR_UNSUPPORTED, "head_dim %d unsupported (only 256)", head_dim);
   if (slot_bytes != uq::kSlotBytes) return fail(UQ_ERR_INVALID_ARG, "slot_bytes %d != 272", slot_bytes);
@@ -213,13 +219,16 @@ uq_status uq_decode(const void* query, const void* kv_cache, const int32_t* bloc
   if ((int64_t)B * Hq * max_num_kv_splits > ((int64_t)1 << 30))
     return fail(UQ_ERR_INVALID_ARG, "B * Hq * max_num_kv_splits exceeds 2^30");
   if (!(scale == scale)) return fail(UQ_ERR_INVALID_ARG, "scale is NaN");
-  if (B == 0) return ok();
-  if (!query || !kv_cache || !block_table || !seq_lens || !workspace || !out)
+  if (B == 0) {
+    *noop = true;
+    return UQ_OK;
+  }
+  if (!query || !kv_cache || !block_table || !workspace || !out)
     return fail(UQ_ERR_INVALID_ARG, "null pointer argument");
   if (!aligned(query, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(workspace, 16))
     return fail(UQ_ERR_INVALID_ARG, "query, kv_cache, workspace and out must be 16-byte aligned");
-  if (!aligned(block_table, 4) || !aligned(seq_lens, 4))
-    return fail(UQ_ERR_INVALID_ARG, "block_table and seq_lens must be 4-byte aligned");
+  if (!aligned(block_table, 4))
+    return fail(UQ_ERR_INVALID_ARG, "block_table must be 4-byte aligned");
   if (q_stride_head < head_dim || q_stride_seq < (int64_t)(Hq - 1) * q_stride_head + head_dim ||
       q_stride_head % 8 || q_stride_seq % 8)
     return fail(UQ_ERR_INVALID_ARG, "query strides (%lld, %lld) must cover a [Hq][256] row and be multiples of 8",
@@ -227,17 +236,68 @@ uq_status uq_decode(const void* query, const void* kv_cache, const int32_t* bloc
   const size_t need = uq_decode_workspace_bytes(B, Hq, head_dim, max_num_kv_splits);
   if (workspace_bytes < need)
     return fail(UQ_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu required", workspace_bytes, need);
+  return UQ_OK;
+}
+
+uq_status launch_checked_decode(const void* query, const void* kv_cache, const int32_t* block_table,
+                                const uq::SeqRows& rows, float scale, int max_num_kv_splits,
+                                void* workspace, void* out, int B, int Hq, int Hk, int num_blocks,
+                                int max_blocks_per_seq, int64_t q_stride_seq, int64_t q_stride_head,
+                                void* stream) {
   unsigned int* err = nullptr;
   uq_status st = error_word(&err);
   if (st != UQ_OK) return st;
   cudaError_t e = uq::launch_decode(static_cast<const uint16_t*>(query), q_stride_seq, q_stride_head,
-                                    static_cast<const uint8_t*>(kv_cache), block_table, seq_lens, scale,
+                                    static_cast<const uint8_t*>(kv_cache), block_table, rows, scale,
                                     B, Hq, Hk, num_blocks, max_blocks_per_seq, max_num_kv_splits,
                                     workspace, static_cast<uint16_t*>(out), err,
                                     static_cast<cudaStream_t>(stream), g_ev_before_stage1,
                                     g_ev_after_stage1);
   if (e != cudaSuccess) return fail(UQ_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
   return ok();
+}
+
+}  // namespace
+
+uq_status uq_decode(const void* query, const void* kv_cache, const int32_t* block_table,
+                    const int32_t* seq_lens, float scale, int max_num_kv_splits, void* workspace,
+                    size_t workspace_bytes, void* out, int B, int Hq, int Hk, int head_dim,
+                    int num_blocks, int block_size, int max_blocks_per_seq, int slot_bytes,
+                    int64_t q_stride_seq, int64_t q_stride_head, void* stream) {
+  bool noop = false;
+  uq_status st = check_decode(query, kv_cache, block_table, scale, max_num_kv_splits, workspace,
+                              workspace_bytes, out, B, Hq, Hk, head_dim, num_blocks, block_size,
+                              max_blocks_per_seq, slot_bytes, q_stride_seq, q_stride_head, &noop);
+  if (st != UQ_OK) return st;
+  if (noop) return ok();
+  if (!seq_lens) return fail(UQ_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(seq_lens, 4)) return fail(UQ_ERR_INVALID_ARG, "block_table and seq_lens must be 4-byte aligned");
+  const uq::SeqRows rows{seq_lens, (int64_t)max_blocks_per_seq, -1};
+  return launch_checked_decode(query, kv_cache, block_table, rows, scale, max_num_kv_splits, workspace,
+                               out, B, Hq, Hk, num_blocks, max_blocks_per_seq, q_stride_seq,
+                               q_stride_head, stream);
+}
+
+uq_status uq_decode_multi_query(const void* query, const void* kv_cache, const int32_t* block_table,
+                                int cached_len, int q_len, float scale, int max_num_kv_splits,
+                                void* workspace, size_t workspace_bytes, void* out, int Hq, int Hk,
+                                int head_dim, int num_blocks, int block_size, int max_blocks_per_seq,
+                                int slot_bytes, int64_t q_stride_tok, int64_t q_stride_head,
+                                void* stream) {
+  if (cached_len < 0) return fail(UQ_ERR_INVALID_ARG, "cached_len %d < 0", cached_len);
+  bool noop = false;
+  uq_status st = check_decode(query, kv_cache, block_table, scale, max_num_kv_splits, workspace,
+                              workspace_bytes, out, q_len, Hq, Hk, head_dim, num_blocks, block_size,
+                              max_blocks_per_seq, slot_bytes, q_stride_tok, q_stride_head, &noop);
+  if (st != UQ_OK) return st;
+  if (noop) return ok();
+  if ((int64_t)cached_len + q_len > (int64_t)max_blocks_per_seq * block_size)
+    return fail(UQ_ERR_INVALID_ARG, "cached_len %d + q_len %d exceeds the %d pages of block_table",
+                cached_len, q_len, max_blocks_per_seq);
+  const uq::SeqRows rows{nullptr, 0, cached_len};
+  return launch_checked_decode(query, kv_cache, block_table, rows, scale, max_num_kv_splits, workspace,
+                               out, q_len, Hq, Hk, num_blocks, max_blocks_per_seq, q_stride_tok,
+                               q_stride_head, stream);
 }
 
 uq_status uq_check_device_error(void* stream, unsigned int* flags_out) {

@@ -48,7 +48,7 @@ namespace uq {
 // Plan.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kPlanThreads)
-decode_plan(const int32_t* __restrict__ seq_lens, int B, int Hk, int S, int max_blocks,
+decode_plan(const SeqRows rows, int B, int Hk, int S, int max_blocks,
             int target_units, Workspace ws) {
   __shared__ long long s_part[kPlanThreads / 32];
   __shared__ int s_hist[32], s_cursor[32], s_wsum[kPlanThreads / 32];
@@ -58,7 +58,7 @@ decode_plan(const int32_t* __restrict__ seq_lens, int B, int Hk, int S, int max_
   if (tid < 32) s_hist[tid] = 0;
 
   long long mine = 0;
-  for (int b = tid; b < B; b += kPlanThreads) mine += (clamp_len(seq_lens[b], max_blocks) + kPage - 1) / kPage;
+  for (int b = tid; b < B; b += kPlanThreads) mine += (row_len(rows, b, max_blocks) + kPage - 1) / kPage;
 #pragma unroll
   for (int m = 16; m > 0; m >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, m);
   if (lane == 0) s_part[warp] = mine;
@@ -74,7 +74,7 @@ decode_plan(const int32_t* __restrict__ seq_lens, int B, int Hk, int S, int max_
   if (T < kMinPagesPerUnit) T = kMinPagesPerUnit;
 
   for (int b = tid; b < B; b += kPlanThreads) {
-    const int P = (clamp_len(seq_lens[b], max_blocks) + kPage - 1) / kPage;
+    const int P = (row_len(rows, b, max_blocks) + kPage - 1) / kPage;
     int n = 0, pps = 0, nact = 0;
     if (P > 0) {
       const long long want = (P + T - 1) / T;
@@ -171,7 +171,7 @@ template <int NT, int NWARPS, int NSTAGE>
 __global__ void __launch_bounds__(NWARPS * 32, NT == 1 ? UQ_S1_MIN_BLOCKS : 2)
 decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
               const __grid_constant__ CUtensorMap kv_map, const int32_t* __restrict__ block_table,
-              const int32_t* __restrict__ seq_lens, float scale_log2e, int Hq, int Hk,
+              const SeqRows rows, float scale_log2e, int Hq, int Hk,
               int QG, int num_blocks, int max_blocks, int S, Workspace ws,
               unsigned* __restrict__ err) {
   using Lay = Stage1Layout<NT, NWARPS, NSTAGE>;
@@ -211,7 +211,7 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
     if (u >= n_units || s_misc[1]) break;
     const uint32_t unit = ws.units[u];
     const int b = (int)(unit & 0xffffu), split = (int)((unit >> 16) & 0xffu), g = (int)(unit >> 24);
-    const int L = clamp_len(seq_lens[b], max_blocks);
+    const int L = row_len(rows, b, max_blocks);
     const int pps = ws.seq_info[b].x;
     const int P = (L + kPage - 1) / kPage;
     const int p_begin = split * pps;
@@ -220,7 +220,7 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
     // ---- per-warp page schedule ---------------------------------------------
     const int n_pages = p_end - p_begin;
     const int n_my = n_pages > warp ? (n_pages - warp + NWARPS - 1) / NWARPS : 0;
-    const int32_t* bt_row = block_table + (int64_t)b * max_blocks + p_begin + warp;
+    const int32_t* bt_row = block_table + (int64_t)b * rows.bt_stride + p_begin + warp;
     int pid_chunk = -1, pid_reg = -1;
 
     auto issue = [&](int j, int stg) {
@@ -699,7 +699,7 @@ static cudaError_t make_kv_tensor_map(CUtensorMap* map, const uint8_t* kv, int H
 // Plan, then stage 1 (bracketed by the caller's timing events, if any).
 template <int NT>
 static cudaError_t launch_plan_and_stage1(const uint16_t* query, int64_t q_ss, int64_t q_sh,
-                                          const uint8_t* kv, const int32_t* bt, const int32_t* sl,
+                                          const uint8_t* kv, const int32_t* bt, const SeqRows& sl,
                                           float scale, int B, int Hq, int Hk, int num_blocks,
                                           int max_blocks, int S, const Workspace& ws, unsigned* err,
                                           cudaStream_t stream, cudaEvent_t ev_before,
@@ -725,7 +725,7 @@ static cudaError_t launch_plan_and_stage1(const uint16_t* query, int64_t q_ss, i
 size_t decode_workspace_bytes(int B, int Hq, int S) { return workspace_bytes(B, Hq, S); }
 
 cudaError_t launch_decode(const uint16_t* query, int64_t q_ss, int64_t q_sh, const uint8_t* kv,
-                          const int32_t* bt, const int32_t* sl, float scale, int B, int Hq,
+                          const int32_t* bt, const SeqRows& sl, float scale, int B, int Hq,
                           int Hk, int num_blocks, int max_blocks, int S, void* workspace,
                           uint16_t* out, unsigned* err, cudaStream_t stream,
                           cudaEvent_t ev_before_stage1, cudaEvent_t ev_after_stage1) {

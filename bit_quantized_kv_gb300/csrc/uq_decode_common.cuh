@@ -76,6 +76,21 @@ __device__ __forceinline__ int clamp_len(int L, int max_blocks) {
   return (long long)L > cap ? (int)cap : L;
 }
 
+// Where the decode kernels find each row's length and pages.  A batch reads
+// seq_lens[b] and block-table row b (bt_stride = the table's width).  A
+// multi-query chunk (mq_base >= 0) gives row b the length mq_base + b + 1
+// and every row the same pages (bt_stride = 0), as the synthetic lengths
+// arange(cached + 1, L + 1) and expanded block table of a continuation chunk.
+struct SeqRows {
+  const int32_t* seq_lens;
+  int64_t bt_stride;
+  int mq_base;
+};
+
+__device__ __forceinline__ int row_len(const SeqRows& r, int b, int max_blocks) {
+  return clamp_len(r.mq_base >= 0 ? r.mq_base + b + 1 : r.seq_lens[b], max_blocks);
+}
+
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1,
                                             uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"

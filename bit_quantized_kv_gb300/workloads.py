@@ -172,6 +172,12 @@ def query(wl: DecodeWorkload, device="cpu", step: int = 0) -> torch.Tensor:
     return _randn_bf16((wl.B, wl.Hq, wl.D), gen, device)
 
 
+def chunk_query(wl: DecodeWorkload, q_len: int, device="cpu", step: int = 0) -> torch.Tensor:
+    """bf16 query [q_len, Hq, D] of a continuation chunk of sequence 0."""
+    gen = _gen(device, wl.seed * 1_000_003 + 333_331 + 7 * step)
+    return _randn_bf16((q_len, wl.Hq, wl.D), gen, device)
+
+
 def new_token_kv(wl: DecodeWorkload, device="cpu", step: int = 0):
     """bf16 K, V [B, Hk, D] of the token each sequence appends at a decode step."""
     gen = _gen(device, wl.seed * 1_000_003 + 499_979 + 7 * step)
@@ -254,3 +260,18 @@ def dequant_bytes(wl: DecodeWorkload) -> int:
     pages = int((int(wl.seq_lens[0]) + wl.block_size - 1) // wl.block_size)
     rows = pages * wl.block_size * wl.Hk
     return rows * (wl.D + wl.D // 16) + rows * wl.D * 2 * 2 + pages * 4
+
+
+def multi_query_workload(name: str = "mq"):
+    """A continuation chunk of q_len tokens after cached_len cached tokens of
+    one sequence (all cached_len + q_len tokens stored); returns (wl, cached_len, q_len).
+
+    mq   cached 131072 + 8 draft tokens, Hq=64, Hk=8 (GQA 8), S=32, seed 8
+    """
+    if name == "mq":
+        cached, q_len = 131072, 8
+        L = cached + q_len
+        wl = make_decode_workload("mq", 1, 64, 8, np.array([L]), (L + BLOCK_SIZE - 1) // BLOCK_SIZE, 32,
+                                  seed=8)
+        return wl, cached, q_len
+    raise KeyError(name)

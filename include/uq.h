@@ -17,8 +17,9 @@
  *
  * Conventions shared by every entry point
  *   - All tensor arguments are DEVICE pointers owned by the caller.  The
- *     library allocates no memory and never synchronises inside uq_store,
- *     uq_store_rotated_f32 or uq_decode; work is enqueued on `stream`
+ *     library allocates no memory and never synchronises inside its compute
+ *     calls (uq_store, uq_store_rotated_f32, uq_decode,
+ *     uq_decode_multi_query, uq_full_dequant); work is enqueued on `stream`
  *     (a cudaStream_t passed as void*; NULL is the legacy default stream).
  *   - Arguments are validated on the host before anything is enqueued; an
  *     invalid call returns an error code and enqueues nothing.  The message
@@ -170,6 +171,39 @@ uq_status uq_decode(const void *query, const void *kv_cache,
                     int head_dim, int num_blocks, int block_size,
                     int max_blocks_per_seq, int slot_bytes, int64_t q_stride_seq,
                     int64_t q_stride_head, void *stream);
+
+/*
+ * uq_decode_multi_query -- attention of a short continuation chunk (or of
+ * the draft tokens of speculative decoding) over the FP4 cache
+ * (ultraquant_attn, UltraQuantAttentionImpl._prefill_attention, continuation
+ * chunks with q_len <= _CONTINUATION_DECODE_THRESHOLD: the decode-shaped
+ * kernel run on synthetic seq_lens = arange(cached_len + 1, seq_len + 1) and
+ * the sequence's block-table row expanded q_len times).
+ *
+ *   query        bf16, row i of the chunk (its token at absolute position
+ *                cached_len + i) and query head r at i * q_stride_tok +
+ *                r * q_stride_head + d.
+ *   kv_cache     uint8 cache that already holds the sequence's first
+ *                cached_len + q_len tokens, the chunk's own K/V included
+ *                (written by uq_store before the call).
+ *   block_table  int32 [max_blocks_per_seq]: the one sequence's page ids.
+ *   workspace    uq_decode_workspace_bytes(q_len, Hq, D, S) bytes.
+ *   out          bf16 [q_len][Hq][D] contiguous, written.
+ *
+ * Row i attends causally to tokens 0 .. cached_len + i: exactly uq_decode
+ * on a batch of q_len rows with seq_lens[i] = cached_len + i + 1 that all
+ * read the same pages, without materialising those arrays.  Pages shared by
+ * the rows are read from HBM once and served to the other rows from L2.
+ * Requires cached_len >= 0 and cached_len + q_len <= max_blocks_per_seq *
+ * block_size; q_len == 0 is a no-op.  Other rules as uq_decode.
+ */
+uq_status uq_decode_multi_query(const void *query, const void *kv_cache,
+                                const int32_t *block_table, int cached_len, int q_len,
+                                float scale, int max_num_kv_splits, void *workspace,
+                                size_t workspace_bytes, void *out, int Hq, int Hk,
+                                int head_dim, int num_blocks, int block_size,
+                                int max_blocks_per_seq, int slot_bytes,
+                                int64_t q_stride_tok, int64_t q_stride_head, void *stream);
 
 /*
  * uq_full_dequant -- expand one sequence's cached prefix to bf16

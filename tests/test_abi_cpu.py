@@ -132,6 +132,35 @@ def test_store_rotated_rejects_invalid_arguments(lib):
     assert st == binding.UQ_ERR_INVALID_ARG
 
 
+def _mq(lib, **kw):
+    args = dict(q=FAKE, kv=FAKE, bt=FAKE, cached=100, q_len=4, scale=0.0625, S=8, ws=FAKE,
+                ws_bytes=1 << 30, out=FAKE, Hq=16, Hk=2, D=256, nb=64, bs=16, mb=8, sb=272,
+                qst=16 * 256, qsh=256)
+    args.update(kw)
+    return lib.uq_decode_multi_query(args["q"], args["kv"], args["bt"], args["cached"], args["q_len"],
+                                     args["scale"], args["S"], args["ws"], args["ws_bytes"], args["out"],
+                                     args["Hq"], args["Hk"], args["D"], args["nb"], args["bs"], args["mb"],
+                                     args["sb"], args["qst"], args["qsh"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(cached=-1), binding.UQ_ERR_INVALID_ARG),
+    (dict(cached=126, q_len=3), binding.UQ_ERR_INVALID_ARG),   # 129 tokens > 8 pages
+    (dict(q_len=-1), binding.UQ_ERR_INVALID_ARG),
+    (dict(Hq=20), binding.UQ_ERR_UNSUPPORTED),                 # GQA 10
+    (dict(ws_bytes=100), binding.UQ_ERR_WORKSPACE_TOO_SMALL),
+    (dict(q=FAKE + 8), binding.UQ_ERR_INVALID_ARG),
+    (dict(bt=0), binding.UQ_ERR_INVALID_ARG),
+])
+def test_multi_query_rejects_invalid_arguments(lib, kw, status):
+    assert _mq(lib, **kw) == status
+    assert lib.uq_last_error().decode() != ""
+
+
+def test_multi_query_empty_chunk_is_a_noop(lib):
+    assert _mq(lib, q_len=0, q=0, out=0, ws=0) == binding.UQ_OK
+
+
 def _dequant(lib, **kw):
     args = dict(kv=FAKE, bt=FAKE, n=3, k=FAKE, v=FAKE, Hk=2, D=256, nb=4, bs=16, sb=272)
     args.update(kw)
