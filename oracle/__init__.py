@@ -56,6 +56,10 @@ def lib() -> ctypes.CDLL:
                                 c_int, c_int, c_p]
         L.uqo_store_f32.restype = c_i64
         L.uqo_store_f32.argtypes = [c_p, c_p, c_p, c_i64, c_int, c_int, c_int, c_int, c_p]
+        L.uqo_decode_ex.restype = c_int
+        L.uqo_decode_ex.argtypes = [c_p, c_i64, c_i64, c_p, c_p, c_p, c_dbl,
+                                    c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
+                                    c_p, c_int, c_p, c_int, c_int, c_p]
         L.uqo_full_dequant.restype = c_int
         L.uqo_full_dequant.argtypes = [c_p, c_p, c_int, c_int, c_int, c_int, c_int, c_p, c_p]
         L.uqo_query_prime.restype = None
@@ -212,11 +216,13 @@ def query_prime(q_bits: np.ndarray) -> np.ndarray:
 
 def decode(query_bits: np.ndarray, kv_cache: np.ndarray, block_table: np.ndarray,
            seq_lens: np.ndarray, scale: float, splits: int = 0,
-           rows: np.ndarray | None = None, nthreads: int | None = None) -> np.ndarray:
+           rows: np.ndarray | None = None, nthreads: int | None = None,
+           sinks: np.ndarray | None = None, window: int = 0) -> np.ndarray:
     """fp64 decode attention.
 
     query_bits: uint16 [B, Hq, D]; kv_cache: uint8 [nb, bs, Hk, slot];
-    block_table: int32 [B, max_blocks]; seq_lens: int32 [B].
+    block_table: int32 [B, max_blocks]; seq_lens: int32 [B].  Optional sink
+    logits [Hq] and a sliding window (> 0: the last ``window`` tokens).
     Returns fp64 [B, Hq, D], or [len(rows), D] when ``rows`` (an int32 [n, 2]
     array of (b, r) pairs) is given.
     """
@@ -235,9 +241,11 @@ def decode(query_bits: np.ndarray, kv_cache: np.ndarray, block_table: np.ndarray
         rows = np.ascontiguousarray(rows, dtype=np.int32).reshape(-1, 2)
         out = np.zeros((rows.shape[0], D), dtype=np.float64)
         rows_p, n_rows = _ptr(rows), rows.shape[0]
-    rc = lib().uqo_decode(_ptr(q), Hq * D, D, _ptr(kv), _ptr(bt), _ptr(sl), float(scale),
-                          B, Hq, Hk, D, nb, bs, bt.shape[1], int(splits),
-                          rows_p, n_rows, int(nthreads), _ptr(out))
+    sk = None if sinks is None else np.ascontiguousarray(sinks, dtype=np.float64).reshape(Hq)
+    rc = lib().uqo_decode_ex(_ptr(q), Hq * D, D, _ptr(kv), _ptr(bt), _ptr(sl), float(scale),
+                             B, Hq, Hk, D, nb, bs, bt.shape[1], int(splits),
+                             rows_p, n_rows, None if sk is None else _ptr(sk), int(window),
+                             int(nthreads), _ptr(out))
     if rc != 0:
         raise ValueError(f"oracle decode failed ({rc})")
     return out

@@ -32,6 +32,10 @@
  *   uqo_decode          pinned: L=1, equal keys, dominant logit, head map,
  *                       page permutation invariance, numpy brute force
  *   uqo_decode (S > 0)  pinned: equals the single softmax to 1e-12
+ *   uqo_decode_ex       pinned: window >= L equals no window; window 1 gives
+ *                       the last token's v exactly; equal keys with a sink,
+ *                       closed form; sink -> -inf equals no sink; split =
+ *                       unsplit with both; numpy brute force
  *   uqo_full_dequant    pinned: numpy bit-level mirror on tiny caches, spike
  *                       slot, closed forms at scale bytes 0, 254 and 255,
  *                       page-permutation invariance
@@ -403,6 +407,8 @@ typedef struct {
     int S;                      /* 0: one softmax over all tokens */
     const int32_t *rows;        /* (b, r) pairs, or NULL for all B*Hq rows */
     int n_rows;
+    const double *sinks;        /* [Hq] sink logits, or NULL */
+    int window;                 /* > 0: attend to the last `window` tokens only */
     const double *H;
     double *out;                /* [n_rows][D] */
     int status;
@@ -467,7 +473,11 @@ static int attend_range(const decode_args *a, int b, int g, const double *qp,
  * One output row (b, r).  Query head r reads kv head r / (Hq / Hk)
  * [ultraquant_attn: __init__, num_kv_groups].  Without splits this is plain
  * softmax(scale q'.k) v over the sequence's L_b tokens; L_b = 0 gives zeros
- * (reading).  With S splits, split s covers [s c, min((s+1) c, L)) with
+ * (reading).  [ultraquant_attn: sliding_window, sinks, passed on to the
+ * unified attention, window_size = (sliding_window - 1, 0)] -- readings: a
+ * window W > 0 keeps tokens [max(0, L - W), L); a sink logit z_r (same units
+ * as scale q'.k) joins the softmax denominator only:
+ * out = sum_t e^(s_t - m) v_t / (e^(z_r - m) + sum_t e^(s_t - m)).  With S splits, split s covers [s c, min((s+1) c, L)) with
  * c = ceil(L / S), each split keeps (m_s, l_s, o_s), and the splits are merged
  * with the log-sum-exp rule [tq_decode_v2: stage 2; flydsl_decode: reduce
  * partitions]: out = sum_s e^(m_s - M) l_s o_s / sum_s e^(m_s - M) l_s.
@@ -487,17 +497,23 @@ static int decode_row(const decode_args *a, int b, int r, double *out)
         q[d] = a->query[(int64_t)b * a->q_stride_seq + (int64_t)r * a->q_stride_head + d];
     uqo_query_prime(q, D, a->H, qp);
     int rc = 0;
+    int lo = (a->window > 0 && L > a->window) ? L - a->window : 0;
     if (a->S <= 0) {
         double m, l;
-        rc = attend_range(a, b, g, qp, 0, L, &m, &l, out);
+        rc = attend_range(a, b, g, qp, lo, L, &m, &l, out);
+        if (rc == 0 && a->sinks) {
+            double f = l / (l + exp(a->sinks[r] - m));
+            for (int d = 0; d < D; ++d)
+                out[d] *= f;
+        }
     } else {
-        int c = (L + a->S - 1) / a->S;
+        int c = (L - lo + a->S - 1) / a->S;
         double M = -INFINITY;
         double *ms = (double *)malloc(sizeof(double) * a->S);
         double *ls = (double *)malloc(sizeof(double) * a->S);
         double *os = (double *)malloc(sizeof(double) * (size_t)a->S * D);
         for (int s = 0; s < a->S && rc == 0; ++s) {
-            int t0 = s * c, t1 = (s + 1) * c < L ? (s + 1) * c : L;
+            int t0 = lo + s * c, t1 = lo + (s + 1) * c < L ? lo + (s + 1) * c : L;
             if (t0 >= t1) { ms[s] = -INFINITY; ls[s] = 0.0; continue; }
             rc = attend_range(a, b, g, qp, t0, t1, &ms[s], &ls[s], os + (size_t)s * D);
             if (ms[s] > M) M = ms[s];
@@ -511,6 +527,8 @@ static int decode_row(const decode_args *a, int b, int r, double *out)
                 for (int d = 0; d < D; ++d)
                     out[d] += w * os[(size_t)s * D + d];
             }
+            if (a->sinks)
+                den += exp(a->sinks[r] - M);
             for (int d = 0; d < D; ++d)
                 out[d] /= den;
         }
@@ -549,11 +567,12 @@ static void *decode_worker(void *p)
  * arithmetic of a row does not depend on the thread count.
  * Returns 0, or -1 on an out-of-range page id or a table that is too short.
  */
-int uqo_decode(const uint16_t *query, int64_t q_stride_seq, int64_t q_stride_head,
-               const uint8_t *kv_cache, const int32_t *block_table,
-               const int32_t *seq_lens, double scale, int B, int Hq, int Hk,
-               int D, int num_blocks, int block_size, int max_blocks, int S,
-               const int32_t *rows, int n_rows, int nthreads, double *out)
+int uqo_decode_ex(const uint16_t *query, int64_t q_stride_seq, int64_t q_stride_head,
+                  const uint8_t *kv_cache, const int32_t *block_table,
+                  const int32_t *seq_lens, double scale, int B, int Hq, int Hk,
+                  int D, int num_blocks, int block_size, int max_blocks, int S,
+                  const int32_t *rows, int n_rows, const double *sinks, int window,
+                  int nthreads, double *out)
 {
     if (Hk <= 0 || Hq % Hk != 0 || (D & (D - 1)) != 0 || D < 32)
         return -2;
@@ -561,7 +580,7 @@ int uqo_decode(const uint16_t *query, int64_t q_stride_seq, int64_t q_stride_hea
     uqo_hadamard(D, H);
     decode_args a = {query, q_stride_seq, q_stride_head, kv_cache, block_table,
                      seq_lens, scale, B, Hq, Hk, D, num_blocks, block_size,
-                     max_blocks, S, rows, n_rows, H, out, 0};
+                     max_blocks, S, rows, n_rows, sinks, window, H, out, 0};
     if (nthreads < 1) nthreads = 1;
     if (nthreads > 256) nthreads = 256;
     pthread_t tid[256];
@@ -574,4 +593,16 @@ int uqo_decode(const uint16_t *query, int64_t q_stride_seq, int64_t q_stride_hea
         pthread_join(tid[i], NULL);
     free(H);
     return a.status;
+}
+
+/* uqo_decode_ex without sinks and without a window. */
+int uqo_decode(const uint16_t *query, int64_t q_stride_seq, int64_t q_stride_head,
+               const uint8_t *kv_cache, const int32_t *block_table,
+               const int32_t *seq_lens, double scale, int B, int Hq, int Hk,
+               int D, int num_blocks, int block_size, int max_blocks, int S,
+               const int32_t *rows, int n_rows, int nthreads, double *out)
+{
+    return uqo_decode_ex(query, q_stride_seq, q_stride_head, kv_cache, block_table, seq_lens,
+                         scale, B, Hq, Hk, D, num_blocks, block_size, max_blocks, S, rows,
+                         n_rows, NULL, 0, nthreads, out);
 }
