@@ -32,7 +32,8 @@ HEAD_DIM = 256
 SLOT_BYTES = 272
 
 EXPORTED = ("uq_version", "uq_slot_bytes", "uq_decode_workspace_bytes", "uq_store",
-            "uq_store_rotated_f32", "uq_decode", "uq_decode_multi_query", "uq_full_dequant",
+            "uq_store_rotated_f32", "uq_decode", "uq_decode_ex", "uq_decode_multi_query",
+            "uq_full_dequant",
             "uq_decode_static_scratch",
             "uq_set_timing_events", "uq_last_error", "uq_check_device_error")
 
@@ -72,9 +73,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.uq_decode.argtypes = [c_p, c_p, c_p, c_p, c_f, c_int, c_p, c_sz, c_p, c_int, c_int,
                             c_int, c_int, c_int, c_int, c_int, c_int, c_i64, c_i64, c_p]
     L.uq_decode_multi_query.restype = c_int
-    L.uq_decode_multi_query.argtypes = [c_p, c_p, c_p, c_int, c_int, c_f, c_int, c_p, c_sz, c_p,
-                                        c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_i64,
-                                        c_i64, c_p]
+    L.uq_decode_multi_query.argtypes = [c_p, c_p, c_p, c_int, c_int, c_f, c_p, c_int, c_int, c_p,
+                                        c_sz, c_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
+                                        c_i64, c_i64, c_p]
+    L.uq_decode_ex.restype = c_int
+    L.uq_decode_ex.argtypes = [c_p, c_p, c_p, c_p, c_f, c_p, c_int, c_int, c_p, c_sz, c_p, c_int,
+                               c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_i64, c_i64, c_p]
     L.uq_full_dequant.restype = c_int
     L.uq_full_dequant.argtypes = [c_p, c_p, c_int, c_p, c_p, c_int, c_int, c_int, c_int, c_int, c_p]
     L.uq_decode_static_scratch.restype = c_int
@@ -203,9 +207,47 @@ def uq_decode(query: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Te
     return out
 
 
+def uq_decode_ex(query: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
+                 seq_lens: torch.Tensor, scale: float, sinks: torch.Tensor | None,
+                 sliding_window: int, max_num_kv_splits: int, workspace: torch.Tensor,
+                 out: torch.Tensor, stream=None) -> torch.Tensor:
+    """uq_decode with optional sink logits (fp32 [Hq] CUDA tensor or None)
+    and a sliding window (> 0: the last ``sliding_window`` tokens)."""
+    _need(query, "query", torch.bfloat16, 3)
+    _need(kv_cache, "kv_cache", torch.uint8, 4)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(out, "out", torch.bfloat16, 3)
+    if not workspace.is_cuda:
+        raise ValueError("workspace must be a CUDA tensor")
+    B, Hq, D = query.shape
+    if sinks is not None:
+        _need(sinks, "sinks", torch.float32, 1)
+        if sinks.shape[0] != Hq or not sinks.is_contiguous():
+            raise ValueError("sinks must be a contiguous fp32 [Hq] tensor")
+    if query.stride(2) != 1:
+        raise ValueError("query rows must be contiguous along the head dim")
+    if out.shape != query.shape or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor shaped like query")
+    if not (kv_cache.is_contiguous() and block_table.is_contiguous() and seq_lens.is_contiguous()):
+        raise ValueError("kv_cache, block_table and seq_lens must be contiguous")
+    nb, bs, Hk, sb = kv_cache.shape
+    if block_table.shape[0] < B or seq_lens.shape[0] < B:
+        raise ValueError("block_table / seq_lens have fewer rows than the batch")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(load().uq_decode_ex(query.data_ptr(), kv_cache.data_ptr(), block_table.data_ptr(),
+                               seq_lens.data_ptr(), float(scale),
+                               None if sinks is None else sinks.data_ptr(), int(sliding_window),
+                               int(max_num_kv_splits), workspace.data_ptr(), ws_bytes, out.data_ptr(),
+                               B, Hq, Hk, D, nb, bs, block_table.shape[1], sb, query.stride(0),
+                               query.stride(1), _stream_ptr(stream)))
+    return out
+
+
 def uq_decode_multi_query(query: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
                           cached_len: int, scale: float, max_num_kv_splits: int,
-                          workspace: torch.Tensor, out: torch.Tensor, stream=None) -> torch.Tensor:
+                          workspace: torch.Tensor, out: torch.Tensor, stream=None,
+                          sinks: torch.Tensor | None = None, sliding_window: int = 0) -> torch.Tensor:
     """query bf16 [q_len, Hq, D] (the chunk's rows, row-strided allowed);
     kv_cache uint8 [num_blocks, 16, Hk, 272] holding the first cached_len +
     q_len tokens; block_table int32 [max_blocks] (one sequence); workspace
@@ -226,8 +268,14 @@ def uq_decode_multi_query(query: torch.Tensor, kv_cache: torch.Tensor, block_tab
         raise ValueError("kv_cache and block_table must be contiguous")
     nb, bs, Hk, sb = kv_cache.shape
     ws_bytes = workspace.numel() * workspace.element_size()
+    if sinks is not None:
+        _need(sinks, "sinks", torch.float32, 1)
+        if sinks.shape[0] != Hq or not sinks.is_contiguous():
+            raise ValueError("sinks must be a contiguous fp32 [Hq] tensor")
     _check(load().uq_decode_multi_query(query.data_ptr(), kv_cache.data_ptr(), block_table.data_ptr(),
-                                        int(cached_len), q_len, float(scale), int(max_num_kv_splits),
+                                        int(cached_len), q_len, float(scale),
+                                        None if sinks is None else sinks.data_ptr(), int(sliding_window),
+                                        int(max_num_kv_splits),
                                         workspace.data_ptr(), ws_bytes, out.data_ptr(), Hq, Hk, D, nb,
                                         bs, block_table.shape[0], sb, query.stride(0), query.stride(1),
                                         _stream_ptr(stream)))

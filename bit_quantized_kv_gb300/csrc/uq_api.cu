@@ -19,9 +19,9 @@ cudaError_t launch_store(bool rotated_f32, const void* key, const void* value, v
                          int64_t key_stride, int64_t value_stride, int block_size,
                          int64_t num_slots, unsigned* err, cudaStream_t stream);
 cudaError_t launch_decode(const uint16_t* query, int64_t q_ss, int64_t q_sh, const uint8_t* kv,
-                          const int32_t* bt, const SeqRows& sl, float scale, int B, int Hq,
-                          int Hk, int num_blocks, int max_blocks, int S, void* workspace,
-                          uint16_t* out, unsigned* err, cudaStream_t stream,
+                          const int32_t* bt, const SeqRows& sl, float scale, const float* sinks,
+                          int B, int Hq, int Hk, int num_blocks, int max_blocks, int S,
+                          void* workspace, uint16_t* out, unsigned* err, cudaStream_t stream,
                           cudaEvent_t ev_before_stage1, cudaEvent_t ev_after_stage1);
 size_t decode_workspace_bytes(int B, int Hq, int S);
 cudaError_t launch_full_dequant(const uint8_t* kv, const int32_t* block_table, int n_pages, int Hk,
@@ -240,7 +240,8 @@ uq_status check_decode(const void* query, const void* kv_cache, const int32_t* b
 }
 
 uq_status launch_checked_decode(const void* query, const void* kv_cache, const int32_t* block_table,
-                                const uq::SeqRows& rows, float scale, int max_num_kv_splits,
+                                const uq::SeqRows& rows, float scale, const float* sinks,
+                                int max_num_kv_splits,
                                 void* workspace, void* out, int B, int Hq, int Hk, int num_blocks,
                                 int max_blocks_per_seq, int64_t q_stride_seq, int64_t q_stride_head,
                                 void* stream) {
@@ -249,7 +250,7 @@ uq_status launch_checked_decode(const void* query, const void* kv_cache, const i
   if (st != UQ_OK) return st;
   cudaError_t e = uq::launch_decode(static_cast<const uint16_t*>(query), q_stride_seq, q_stride_head,
                                     static_cast<const uint8_t*>(kv_cache), block_table, rows, scale,
-                                    B, Hq, Hk, num_blocks, max_blocks_per_seq, max_num_kv_splits,
+                                    sinks, B, Hq, Hk, num_blocks, max_blocks_per_seq, max_num_kv_splits,
                                     workspace, static_cast<uint16_t*>(out), err,
                                     static_cast<cudaStream_t>(stream), g_ev_before_stage1,
                                     g_ev_after_stage1);
@@ -259,11 +260,12 @@ uq_status launch_checked_decode(const void* query, const void* kv_cache, const i
 
 }  // namespace
 
-uq_status uq_decode(const void* query, const void* kv_cache, const int32_t* block_table,
-                    const int32_t* seq_lens, float scale, int max_num_kv_splits, void* workspace,
-                    size_t workspace_bytes, void* out, int B, int Hq, int Hk, int head_dim,
-                    int num_blocks, int block_size, int max_blocks_per_seq, int slot_bytes,
-                    int64_t q_stride_seq, int64_t q_stride_head, void* stream) {
+uq_status uq_decode_ex(const void* query, const void* kv_cache, const int32_t* block_table,
+                       const int32_t* seq_lens, float scale, const float* sinks, int sliding_window,
+                       int max_num_kv_splits, void* workspace, size_t workspace_bytes, void* out,
+                       int B, int Hq, int Hk, int head_dim, int num_blocks, int block_size,
+                       int max_blocks_per_seq, int slot_bytes, int64_t q_stride_seq,
+                       int64_t q_stride_head, void* stream) {
   bool noop = false;
   uq_status st = check_decode(query, kv_cache, block_table, scale, max_num_kv_splits, workspace,
                               workspace_bytes, out, B, Hq, Hk, head_dim, num_blocks, block_size,
@@ -271,15 +273,27 @@ uq_status uq_decode(const void* query, const void* kv_cache, const int32_t* bloc
   if (st != UQ_OK) return st;
   if (noop) return ok();
   if (!seq_lens) return fail(UQ_ERR_INVALID_ARG, "null pointer argument");
-  if (!aligned(seq_lens, 4)) return fail(UQ_ERR_INVALID_ARG, "block_table and seq_lens must be 4-byte aligned");
-  const uq::SeqRows rows{seq_lens, (int64_t)max_blocks_per_seq, -1};
-  return launch_checked_decode(query, kv_cache, block_table, rows, scale, max_num_kv_splits, workspace,
-                               out, B, Hq, Hk, num_blocks, max_blocks_per_seq, q_stride_seq,
-                               q_stride_head, stream);
+  if (!aligned(seq_lens, 4) || (sinks && !aligned(sinks, 4)))
+    return fail(UQ_ERR_INVALID_ARG, "block_table, seq_lens and sinks must be 4-byte aligned");
+  const uq::SeqRows rows{seq_lens, (int64_t)max_blocks_per_seq, -1, sliding_window};
+  return launch_checked_decode(query, kv_cache, block_table, rows, scale, sinks, max_num_kv_splits,
+                               workspace, out, B, Hq, Hk, num_blocks, max_blocks_per_seq,
+                               q_stride_seq, q_stride_head, stream);
+}
+
+uq_status uq_decode(const void* query, const void* kv_cache, const int32_t* block_table,
+                    const int32_t* seq_lens, float scale, int max_num_kv_splits, void* workspace,
+                    size_t workspace_bytes, void* out, int B, int Hq, int Hk, int head_dim,
+                    int num_blocks, int block_size, int max_blocks_per_seq, int slot_bytes,
+                    int64_t q_stride_seq, int64_t q_stride_head, void* stream) {
+  return uq_decode_ex(query, kv_cache, block_table, seq_lens, scale, nullptr, 0, max_num_kv_splits,
+                      workspace, workspace_bytes, out, B, Hq, Hk, head_dim, num_blocks, block_size,
+                      max_blocks_per_seq, slot_bytes, q_stride_seq, q_stride_head, stream);
 }
 
 uq_status uq_decode_multi_query(const void* query, const void* kv_cache, const int32_t* block_table,
-                                int cached_len, int q_len, float scale, int max_num_kv_splits,
+                                int cached_len, int q_len, float scale, const float* sinks,
+                                int sliding_window, int max_num_kv_splits,
                                 void* workspace, size_t workspace_bytes, void* out, int Hq, int Hk,
                                 int head_dim, int num_blocks, int block_size, int max_blocks_per_seq,
                                 int slot_bytes, int64_t q_stride_tok, int64_t q_stride_head,
@@ -294,10 +308,11 @@ uq_status uq_decode_multi_query(const void* query, const void* kv_cache, const i
   if ((int64_t)cached_len + q_len > (int64_t)max_blocks_per_seq * block_size)
     return fail(UQ_ERR_INVALID_ARG, "cached_len %d + q_len %d exceeds the %d pages of block_table",
                 cached_len, q_len, max_blocks_per_seq);
-  const uq::SeqRows rows{nullptr, 0, cached_len};
-  return launch_checked_decode(query, kv_cache, block_table, rows, scale, max_num_kv_splits, workspace,
-                               out, q_len, Hq, Hk, num_blocks, max_blocks_per_seq, q_stride_tok,
-                               q_stride_head, stream);
+  if (sinks && !aligned(sinks, 4)) return fail(UQ_ERR_INVALID_ARG, "sinks must be 4-byte aligned");
+  const uq::SeqRows rows{nullptr, 0, cached_len, sliding_window};
+  return launch_checked_decode(query, kv_cache, block_table, rows, scale, sinks, max_num_kv_splits,
+                               workspace, out, q_len, Hq, Hk, num_blocks, max_blocks_per_seq,
+                               q_stride_tok, q_stride_head, stream);
 }
 
 uq_status uq_check_device_error(void* stream, unsigned int* flags_out) {

@@ -58,7 +58,7 @@ decode_plan(const SeqRows rows, int B, int Hk, int S, int max_blocks,
   if (tid < 32) s_hist[tid] = 0;
 
   long long mine = 0;
-  for (int b = tid; b < B; b += kPlanThreads) mine += (row_len(rows, b, max_blocks) + kPage - 1) / kPage;
+  for (int b = tid; b < B; b += kPlanThreads) mine += row_pages(rows, b, max_blocks);
 #pragma unroll
   for (int m = 16; m > 0; m >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, m);
   if (lane == 0) s_part[warp] = mine;
@@ -74,7 +74,7 @@ decode_plan(const SeqRows rows, int B, int Hk, int S, int max_blocks,
   if (T < kMinPagesPerUnit) T = kMinPagesPerUnit;
 
   for (int b = tid; b < B; b += kPlanThreads) {
-    const int P = (row_len(rows, b, max_blocks) + kPage - 1) / kPage;
+    const int P = row_pages(rows, b, max_blocks);
     int n = 0, pps = 0, nact = 0;
     if (P > 0) {
       const long long want = (P + T - 1) / T;
@@ -214,7 +214,8 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
     const int L = row_len(rows, b, max_blocks);
     const int pps = ws.seq_info[b].x;
     const int P = (L + kPage - 1) / kPage;
-    const int p_begin = split * pps;
+    const int lo = row_lo(rows, L);   // first token of the window
+    const int p_begin = lo / kPage + split * pps;
     const int p_end = min(p_begin + pps, P);
 
     // ---- per-warp page schedule ---------------------------------------------
@@ -402,7 +403,8 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
         //    when a page's maximum exceeds the reference by more than
         //    kLazyMaxLog2, so a probability stays below 2^kLazyMaxLog2 (f16 keeps
         //    its full relative precision there) and rescaling O is rare.
-        const bool v0 = gq < nvalid, v1 = gq + 8 < nvalid;
+        const int first = lo - page * kPage;   // window start within this page
+        const bool v0 = gq < nvalid && gq >= first, v1 = gq + 8 < nvalid && gq + 8 >= first;
         uint32_t pw[NT][2];
         bool rescale = false;
         float mu_prev[NT][2];
@@ -592,7 +594,8 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
 // Stage 2: merge the active splits of each (sequence, query head).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(128)
-decode_stage2(Workspace ws, int B, int Hq, int S, uint16_t* __restrict__ out) {
+decode_stage2(Workspace ws, int B, int Hq, int S, const float* __restrict__ sinks,
+              uint16_t* __restrict__ out) {
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
   if (row >= B * Hq) return;
@@ -603,8 +606,11 @@ decode_stage2(Workspace ws, int B, int Hq, int S, uint16_t* __restrict__ out) {
   for (int s = lane; s < n; s += 32) mx = fmaxf(mx, lse[s]);
 #pragma unroll
   for (int msk = 16; msk > 0; msk >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, msk));
+  // a sink logit joins the denominator only (log2 units like the partials)
+  const float zs = sinks ? sinks[row % Hq] * kLog2e : -INFINITY;
+  mx = fmaxf(mx, zs);
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  float den = 0.f;
+  float den = sinks ? fast_exp2(zs - mx) : 0.f;
   if (n > 0 && mx > -INFINITY) {
     const float* po = ws.part_o + (int64_t)row * S * kHeadDim + lane * 8;
     for (int s0 = 0; s0 < n; s0 += 32) {
@@ -620,7 +626,7 @@ decode_stage2(Workspace ws, int B, int Hq, int S, uint16_t* __restrict__ out) {
       }
     }
   }
-  const float inv = den > 0.f ? 1.f / den : 0.f;
+  const float inv = (n > 0 && den > 0.f) ? 1.f / den : 0.f;
   uint32_t pk[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -725,9 +731,9 @@ static cudaError_t launch_plan_and_stage1(const uint16_t* query, int64_t q_ss, i
 size_t decode_workspace_bytes(int B, int Hq, int S) { return workspace_bytes(B, Hq, S); }
 
 cudaError_t launch_decode(const uint16_t* query, int64_t q_ss, int64_t q_sh, const uint8_t* kv,
-                          const int32_t* bt, const SeqRows& sl, float scale, int B, int Hq,
-                          int Hk, int num_blocks, int max_blocks, int S, void* workspace,
-                          uint16_t* out, unsigned* err, cudaStream_t stream,
+                          const int32_t* bt, const SeqRows& sl, float scale, const float* sinks,
+                          int B, int Hq, int Hk, int num_blocks, int max_blocks, int S,
+                          void* workspace, uint16_t* out, unsigned* err, cudaStream_t stream,
                           cudaEvent_t ev_before_stage1, cudaEvent_t ev_after_stage1) {
   const Workspace ws = workspace_layout(workspace, B, Hq, S);
   cudaError_t e =
@@ -738,7 +744,7 @@ cudaError_t launch_decode(const uint16_t* query, int64_t q_ss, int64_t q_sh, con
                                       max_blocks, S, ws, err, stream, ev_before_stage1, ev_after_stage1);
   if (e != cudaSuccess) return e;
   const int rows = B * Hq;
-  decode_stage2<<<(rows + 3) / 4, 128, 0, stream>>>(ws, B, Hq, S, out);
+  decode_stage2<<<(rows + 3) / 4, 128, 0, stream>>>(ws, B, Hq, S, sinks, out);
   return cudaGetLastError();
 }
 

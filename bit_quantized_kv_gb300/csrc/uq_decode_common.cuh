@@ -81,14 +81,27 @@ __device__ __forceinline__ int clamp_len(int L, int max_blocks) {
 // multi-query chunk (mq_base >= 0) gives row b the length mq_base + b + 1
 // and every row the same pages (bt_stride = 0), as the synthetic lengths
 // arange(cached + 1, L + 1) and expanded block table of a continuation chunk.
+// A sliding window (window > 0) keeps the last `window` tokens of each row.
 struct SeqRows {
   const int32_t* seq_lens;
   int64_t bt_stride;
   int mq_base;
+  int window;
 };
 
 __device__ __forceinline__ int row_len(const SeqRows& r, int b, int max_blocks) {
   return clamp_len(r.mq_base >= 0 ? r.mq_base + b + 1 : r.seq_lens[b], max_blocks);
+}
+
+// First token a row of length L attends to.
+__device__ __forceinline__ int row_lo(const SeqRows& r, int L) {
+  return (r.window > 0 && L > r.window) ? L - r.window : 0;
+}
+
+// Pages a row reads: [row_lo / kPage, ceil(L / kPage)).
+__device__ __forceinline__ int row_pages(const SeqRows& r, int b, int max_blocks) {
+  const int L = row_len(r, b, max_blocks);
+  return (L + kPage - 1) / kPage - row_lo(r, L) / kPage;
 }
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1,

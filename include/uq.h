@@ -18,7 +18,7 @@
  * Conventions shared by every entry point
  *   - All tensor arguments are DEVICE pointers owned by the caller.  The
  *     library allocates no memory and never synchronises inside its compute
- *     calls (uq_store, uq_store_rotated_f32, uq_decode,
+ *     calls (uq_store, uq_store_rotated_f32, uq_decode, uq_decode_ex,
  *     uq_decode_multi_query, uq_full_dequant); work is enqueued on `stream`
  *     (a cudaStream_t passed as void*; NULL is the legacy default stream).
  *   - Arguments are validated on the host before anything is enqueued; an
@@ -173,6 +173,31 @@ uq_status uq_decode(const void *query, const void *kv_cache,
                     int64_t q_stride_head, void *stream);
 
 /*
+ * uq_decode_ex -- uq_decode with attention sinks and a sliding window
+ * (ultraquant_attn, UltraQuantAttentionImpl: sinks and sliding_window, which
+ * the backend hands to its unified attention with window_size =
+ * (sliding_window - 1, 0); the FlyDSL kernel rejects both).
+ *
+ *   sinks           fp32 [Hq] device array of sink logits, or NULL.  Query
+ *                   head r's softmax becomes e^(s_t - m) / (e^(z_r - m) +
+ *                   sum_t e^(s_t - m)): the sink z_r (same units as
+ *                   scale * q'.k, finite or -inf) joins the denominator only.
+ *   sliding_window  W > 0: a row of length L attends to tokens
+ *                   [max(0, L - W), L) only; W <= 0: no window.
+ *
+ * Everything else as uq_decode, which is uq_decode_ex(..., NULL, 0, ...).
+ * The window moves the pages a row reads, so the work list (and the time)
+ * shrinks with it.
+ */
+uq_status uq_decode_ex(const void *query, const void *kv_cache,
+                       const int32_t *block_table, const int32_t *seq_lens,
+                       float scale, const float *sinks, int sliding_window,
+                       int max_num_kv_splits, void *workspace, size_t workspace_bytes,
+                       void *out, int B, int Hq, int Hk, int head_dim, int num_blocks,
+                       int block_size, int max_blocks_per_seq, int slot_bytes,
+                       int64_t q_stride_seq, int64_t q_stride_head, void *stream);
+
+/*
  * uq_decode_multi_query -- attention of a short continuation chunk (or of
  * the draft tokens of speculative decoding) over the FP4 cache
  * (ultraquant_attn, UltraQuantAttentionImpl._prefill_attention, continuation
@@ -194,12 +219,15 @@ uq_status uq_decode(const void *query, const void *kv_cache,
  * on a batch of q_len rows with seq_lens[i] = cached_len + i + 1 that all
  * read the same pages, without materialising those arrays.  Pages shared by
  * the rows are read from HBM once and served to the other rows from L2.
- * Requires cached_len >= 0 and cached_len + q_len <= max_blocks_per_seq *
- * block_size; q_len == 0 is a no-op.  Other rules as uq_decode.
+ * sinks and sliding_window as in uq_decode_ex; the window counts back from
+ * each row's own position.  Requires cached_len >= 0 and cached_len + q_len
+ * <= max_blocks_per_seq * block_size; q_len == 0 is a no-op.  Other rules as
+ * uq_decode.
  */
 uq_status uq_decode_multi_query(const void *query, const void *kv_cache,
                                 const int32_t *block_table, int cached_len, int q_len,
-                                float scale, int max_num_kv_splits, void *workspace,
+                                float scale, const float *sinks, int sliding_window,
+                                int max_num_kv_splits, void *workspace,
                                 size_t workspace_bytes, void *out, int Hq, int Hk,
                                 int head_dim, int num_blocks, int block_size,
                                 int max_blocks_per_seq, int slot_bytes,

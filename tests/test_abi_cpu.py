@@ -138,7 +138,8 @@ def _mq(lib, **kw):
                 qst=16 * 256, qsh=256)
     args.update(kw)
     return lib.uq_decode_multi_query(args["q"], args["kv"], args["bt"], args["cached"], args["q_len"],
-                                     args["scale"], args["S"], args["ws"], args["ws_bytes"], args["out"],
+                                     args["scale"], args.get("sinks"), args.get("window", 0), args["S"],
+                                     args["ws"], args["ws_bytes"], args["out"],
                                      args["Hq"], args["Hk"], args["D"], args["nb"], args["bs"], args["mb"],
                                      args["sb"], args["qst"], args["qsh"], None)
 
@@ -151,6 +152,7 @@ def _mq(lib, **kw):
     (dict(ws_bytes=100), binding.UQ_ERR_WORKSPACE_TOO_SMALL),
     (dict(q=FAKE + 8), binding.UQ_ERR_INVALID_ARG),
     (dict(bt=0), binding.UQ_ERR_INVALID_ARG),
+    (dict(sinks=FAKE + 2), binding.UQ_ERR_INVALID_ARG),
 ])
 def test_multi_query_rejects_invalid_arguments(lib, kw, status):
     assert _mq(lib, **kw) == status
