@@ -24,9 +24,9 @@ cudaError_t launch_decode(const uint16_t* query, int64_t q_ss, int64_t q_sh, con
                           void* workspace, uint16_t* out, unsigned* err, cudaStream_t stream,
                           cudaEvent_t ev_before_stage1, cudaEvent_t ev_after_stage1);
 size_t decode_workspace_bytes(int B, int Hq, int S);
-cudaError_t launch_full_dequant(const uint8_t* kv, const int32_t* block_table, int n_pages, int Hk,
-                                int num_blocks, uint16_t* k_out, uint16_t* v_out, unsigned* err,
-                                cudaStream_t stream);
+cudaError_t launch_full_dequant(const uint8_t* kv, const int32_t* block_table, int n_pages,
+                                int lg_tpp, int Hk, int num_blocks, uint16_t* k_out, uint16_t* v_out,
+                                unsigned* err, cudaStream_t stream);
 }  // namespace uq
 
 namespace {
@@ -58,6 +58,15 @@ uq_status ok() {
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Page sizes the decode and dequant kernels walk in whole 16-token tiles.
+bool block_size_ok(int bs) { return bs == 16 || bs == 32 || bs == 64 || bs == 128 || bs == 256; }
+
+int log2_tiles_per_page(int bs) {
+  int lg = 0;
+  while ((16 << lg) < bs) ++lg;
+  return lg;
+}
 
 // Device address of the error word on the current device (set-up on first use).
 uq_status error_word(unsigned int** out) {
@@ -169,13 +178,15 @@ uq_status uq_full_dequant(const void* kv_cache, const int32_t* block_table, int 
                           void* k_out, void* v_out, int Hk, int head_dim, int num_blocks,
                           int block_size, int slot_bytes, void* stream) {
   if (head_dim != uq::kHeadDim) return fail(UQ_ERR_UNSUPPORTED, "head_dim %d unsupported (only 256)", head_dim);
-  if (block_size != 16) return fail(UQ_ERR_UNSUPPORTED, "block_size %d unsupported (only 16)", block_size);
+  if (!block_size_ok(block_size))
+    return fail(UQ_ERR_UNSUPPORTED, "block_size %d unsupported (16, 32, 64, 128 or 256)", block_size);
   if (slot_bytes != uq::kSlotBytes) return fail(UQ_ERR_INVALID_ARG, "slot_bytes %d != 272", slot_bytes);
   if (Hk < 1 || Hk > 256) return fail(UQ_ERR_UNSUPPORTED, "Hk %d outside [1, 256]", Hk);
   if (num_blocks < 1) return fail(UQ_ERR_INVALID_ARG, "num_blocks %d < 1", num_blocks);
   if (n_pages < 0 || (int64_t)n_pages * block_size >= ((int64_t)1 << 31) ||
-      (int64_t)n_pages * Hk >= ((int64_t)1 << 31))
-    return fail(UQ_ERR_INVALID_ARG, "n_pages %d: need n_pages * block_size and n_pages * Hk < 2^31", n_pages);
+      (int64_t)n_pages * (block_size / 16) * Hk >= ((int64_t)1 << 31))
+    return fail(UQ_ERR_INVALID_ARG,
+                "n_pages %d: need n_pages * block_size and n_pages * (block_size / 16) * Hk < 2^31", n_pages);
   if (n_pages == 0) return ok();
   if (!kv_cache || !block_table || !k_out || !v_out)
     return fail(UQ_ERR_INVALID_ARG, "null pointer argument");
@@ -184,8 +195,11 @@ uq_status uq_full_dequant(const void* kv_cache, const int32_t* block_table, int 
   unsigned int* err = nullptr;
   uq_status st = error_word(&err);
   if (st != UQ_OK) return st;
+  if ((int64_t)num_blocks * block_size >= ((int64_t)1 << 31))
+    return fail(UQ_ERR_INVALID_ARG, "num_blocks * block_size must be < 2^31");
   cudaError_t e = uq::launch_full_dequant(static_cast<const uint8_t*>(kv_cache), block_table, n_pages,
-                                          Hk, num_blocks, static_cast<uint16_t*>(k_out),
+                                          log2_tiles_per_page(block_size), Hk, num_blocks,
+                                          static_cast<uint16_t*>(k_out),
                                           static_cast<uint16_t*>(v_out), err,
                                           static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(UQ_ERR_CUDA, "full dequant launch: %s", cudaGetErrorString(e));
@@ -206,7 +220,8 @@ uq_status check_decode(const void* query, const void* kv_cache, const int32_t* b
   if (B < 0) return fail(UQ_ERR_INVALID_ARG, "B %d < 0", B);
   if (head_dim != uq::kHeadDim) return fail(UQ_ERR_UNSUPPORTED, "head_dim %d unsupported (only 256)", head_dim);
   if (slot_bytes != uq::kSlotBytes) return fail(UQ_ERR_INVALID_ARG, "slot_bytes %d != 272", slot_bytes);
-  if (block_size != 16) return fail(UQ_ERR_UNSUPPORTED, "block_size %d unsupported (only 16)", block_size);
+  if (!block_size_ok(block_size))
+    return fail(UQ_ERR_UNSUPPORTED, "block_size %d unsupported (16, 32, 64, 128 or 256)", block_size);
   if (Hk < 1 || Hq < 1 || Hq % Hk) return fail(UQ_ERR_INVALID_ARG, "Hq %d must be a positive multiple of Hk %d", Hq, Hk);
   const int QG = Hq / Hk;
   if (QG != 6 && QG != 8 && QG != 16) return fail(UQ_ERR_UNSUPPORTED, "query heads per kv head %d unsupported (6, 8, 16)", QG);
@@ -214,6 +229,9 @@ uq_status check_decode(const void* query, const void* kv_cache, const int32_t* b
     return fail(UQ_ERR_INVALID_ARG, "max_num_kv_splits %d outside [1, 256]", max_num_kv_splits);
   if (num_blocks < 1 || max_blocks_per_seq < 1)
     return fail(UQ_ERR_INVALID_ARG, "num_blocks %d / max_blocks_per_seq %d must be >= 1", num_blocks, max_blocks_per_seq);
+  if ((int64_t)num_blocks * block_size >= ((int64_t)1 << 31) ||
+      (int64_t)max_blocks_per_seq * block_size >= ((int64_t)1 << 31))
+    return fail(UQ_ERR_INVALID_ARG, "num_blocks and max_blocks_per_seq times block_size must be < 2^31");
   if (B > 65535) return fail(UQ_ERR_INVALID_ARG, "B %d exceeds 65535", B);
   if (Hk > 256) return fail(UQ_ERR_UNSUPPORTED, "Hk %d exceeds 256", Hk);
   if ((int64_t)B * Hq * max_num_kv_splits > ((int64_t)1 << 30))
@@ -275,7 +293,8 @@ uq_status uq_decode_ex(const void* query, const void* kv_cache, const int32_t* b
   if (!seq_lens) return fail(UQ_ERR_INVALID_ARG, "null pointer argument");
   if (!aligned(seq_lens, 4) || (sinks && !aligned(sinks, 4)))
     return fail(UQ_ERR_INVALID_ARG, "block_table, seq_lens and sinks must be 4-byte aligned");
-  const uq::SeqRows rows{seq_lens, (int64_t)max_blocks_per_seq, -1, sliding_window};
+  const uq::SeqRows rows{seq_lens, (int64_t)max_blocks_per_seq, -1, sliding_window,
+                         log2_tiles_per_page(block_size), max_blocks_per_seq * (block_size / 16)};
   return launch_checked_decode(query, kv_cache, block_table, rows, scale, sinks, max_num_kv_splits,
                                workspace, out, B, Hq, Hk, num_blocks, max_blocks_per_seq,
                                q_stride_seq, q_stride_head, stream);
@@ -309,7 +328,8 @@ uq_status uq_decode_multi_query(const void* query, const void* kv_cache, const i
     return fail(UQ_ERR_INVALID_ARG, "cached_len %d + q_len %d exceeds the %d pages of block_table",
                 cached_len, q_len, max_blocks_per_seq);
   if (sinks && !aligned(sinks, 4)) return fail(UQ_ERR_INVALID_ARG, "sinks must be 4-byte aligned");
-  const uq::SeqRows rows{nullptr, 0, cached_len, sliding_window};
+  const uq::SeqRows rows{nullptr, 0, cached_len, sliding_window, log2_tiles_per_page(block_size),
+                         max_blocks_per_seq * (block_size / 16)};
   return launch_checked_decode(query, kv_cache, block_table, rows, scale, sinks, max_num_kv_splits,
                                workspace, out, q_len, Hq, Hk, num_blocks, max_blocks_per_seq,
                                q_stride_tok, q_stride_head, stream);

@@ -40,6 +40,8 @@
 //
 // Stage 2: one warp per (sequence, query head) merges the active splits with
 // the log-sum-exp rule and writes bf16.
+#include <type_traits>
+
 #include "uq_decode_common.cuh"
 
 namespace uq {
@@ -48,7 +50,7 @@ namespace uq {
 // Plan.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kPlanThreads)
-decode_plan(const SeqRows rows, int B, int Hk, int S, int max_blocks,
+decode_plan(const SeqRows rows, int B, int Hk, int S,
             int target_units, Workspace ws) {
   __shared__ long long s_part[kPlanThreads / 32];
   __shared__ int s_hist[32], s_cursor[32], s_wsum[kPlanThreads / 32];
@@ -58,7 +60,7 @@ decode_plan(const SeqRows rows, int B, int Hk, int S, int max_blocks,
   if (tid < 32) s_hist[tid] = 0;
 
   long long mine = 0;
-  for (int b = tid; b < B; b += kPlanThreads) mine += row_pages(rows, b, max_blocks);
+  for (int b = tid; b < B; b += kPlanThreads) mine += row_pages(rows, b);
 #pragma unroll
   for (int m = 16; m > 0; m >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, m);
   if (lane == 0) s_part[warp] = mine;
@@ -74,7 +76,7 @@ decode_plan(const SeqRows rows, int B, int Hk, int S, int max_blocks,
   if (T < kMinPagesPerUnit) T = kMinPagesPerUnit;
 
   for (int b = tid; b < B; b += kPlanThreads) {
-    const int P = row_pages(rows, b, max_blocks);
+    const int P = row_pages(rows, b);
     int n = 0, pps = 0, nact = 0;
     if (P > 0) {
       const long long want = (P + T - 1) / T;
@@ -167,12 +169,14 @@ struct Stage1Layout {
   static constexpr int kBytes = kQOff + kQBytes;
 };
 
-template <int NT, int NWARPS, int NSTAGE>
+// GEN: a sliding window or pages of more than 16 tokens.  The plain
+// instantiation (block_size 16, no window) folds both away.
+template <int NT, int NWARPS, int NSTAGE, bool GEN>
 __global__ void __launch_bounds__(NWARPS * 32, NT == 1 ? UQ_S1_MIN_BLOCKS : 2)
 decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
               const __grid_constant__ CUtensorMap kv_map, const int32_t* __restrict__ block_table,
               const SeqRows rows, float scale_log2e, int Hq, int Hk,
-              int QG, int num_blocks, int max_blocks, int S, Workspace ws,
+              int QG, int num_blocks, int S, Workspace ws,
               unsigned* __restrict__ err) {
   using Lay = Stage1Layout<NT, NWARPS, NSTAGE>;
   constexpr int NCH = NT == 1 ? 4 : 2;   // independent QK accumulator chains per n-tile
@@ -211,24 +215,28 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
     if (u >= n_units || s_misc[1]) break;
     const uint32_t unit = ws.units[u];
     const int b = (int)(unit & 0xffffu), split = (int)((unit >> 16) & 0xffu), g = (int)(unit >> 24);
-    const int L = row_len(rows, b, max_blocks);
+    const int L = row_len(rows, b);
     const int pps = ws.seq_info[b].x;
     const int P = (L + kPage - 1) / kPage;
-    const int lo = row_lo(rows, L);   // first token of the window
+    const int lo = GEN ? row_lo(rows, L) : 0;   // first token of the window
+    const int lg_tpp = GEN ? rows.lg_tpp : 0;
     const int p_begin = lo / kPage + split * pps;
     const int p_end = min(p_begin + pps, P);
 
     // ---- per-warp page schedule ---------------------------------------------
     const int n_pages = p_end - p_begin;
     const int n_my = n_pages > warp ? (n_pages - warp + NWARPS - 1) / NWARPS : 0;
-    const int32_t* bt_row = block_table + (int64_t)b * rows.bt_stride + p_begin + warp;
+    // tile t of the row is tile t % 2^lg_tpp of page block_table[b][t >> lg_tpp]
+    const int32_t* bt_row = block_table + (int64_t)b * rows.bt_stride;
+    const int tile_mask = (1 << lg_tpp) - 1;
     int pid_chunk = -1, pid_reg = -1;
 
     auto issue = [&](int j, int stg) {
       const int chunk = j >> 5;
+      const int tile = p_begin + warp + j * NWARPS;
       if (chunk != pid_chunk) {
         const int jj = chunk * 32 + lane;
-        pid_reg = jj < n_my ? bt_row[(int64_t)jj * NWARPS] : -1;
+        pid_reg = jj < n_my ? bt_row[(p_begin + warp + jj * NWARPS) >> lg_tpp] : -1;
         pid_chunk = chunk;
       }
       const int pid = __shfl_sync(0xffffffffu, pid_reg, j & 31);
@@ -240,7 +248,8 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
         if (ok) {
           fence_proxy_async_smem();
           mbar_arrive_expect_tx(bar, kTileBytes);
-          tma_load_3d(stage_base + stg * kTileBytes, &kv_map, 0, g, pid * kPage, bar);
+          tma_load_3d(stage_base + stg * kTileBytes, &kv_map, 0, g,
+                      ((pid << lg_tpp) + (tile & tile_mask)) * kPage, bar);
         } else {
           atomicOr(err, kErrBadPage);
           mbar_arrive(bar);
@@ -404,7 +413,8 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
         //    kLazyMaxLog2, so a probability stays below 2^kLazyMaxLog2 (f16 keeps
         //    its full relative precision there) and rescaling O is rare.
         const int first = lo - page * kPage;   // window start within this page
-        const bool v0 = gq < nvalid && gq >= first, v1 = gq + 8 < nvalid && gq + 8 >= first;
+        const bool v0 = gq < nvalid && (!GEN || gq >= first);
+        const bool v1 = gq + 8 < nvalid && (!GEN || gq + 8 >= first);
         uint32_t pw[NT][2];
         bool rescale = false;
         float mu_prev[NT][2];
@@ -653,7 +663,7 @@ static cudaError_t record_timing_event(cudaEvent_t ev, cudaStream_t stream) {
 
 // Per device and instantiation: set the shared-memory opt-in once and size the
 // persistent grid from the occupancy the kernel actually gets.
-template <int NT>
+template <int NT, bool GEN>
 static cudaError_t stage1_grid(int* grid) {
   constexpr int NWARPS = 4, NSTAGE = kStage1Stages;
   using Lay = Stage1Layout<NT, NWARPS, NSTAGE>;
@@ -665,7 +675,7 @@ static cudaError_t stage1_grid(int* grid) {
     *grid = grid_of_device[dev];
     return cudaSuccess;
   }
-  auto kern = decode_stage1<NT, NWARPS, NSTAGE>;
+  auto kern = decode_stage1<NT, NWARPS, NSTAGE, GEN>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
   if (e != cudaSuccess) return e;
   int sms = 0, per_sm = 0;
@@ -679,9 +689,9 @@ static cudaError_t stage1_grid(int* grid) {
 }
 
 // The cache as a 3-D tensor of 32-bit words: x = word within a slot (68),
-// y = kv head (Hk, stride 272 B), z = slot (num_blocks * 16, stride Hk * 272 B).
-// One box of 68 x 1 x 16 words is one (page, kv head) tile.
-static cudaError_t make_kv_tensor_map(CUtensorMap* map, const uint8_t* kv, int Hk, int num_blocks) {
+// y = kv head (Hk, stride 272 B), z = slot (num_blocks * block_size, stride
+// Hk * 272 B).  One box of 68 x 1 x 16 words is one (16-token tile, kv head).
+static cudaError_t make_kv_tensor_map(CUtensorMap* map, const uint8_t* kv, int Hk, int64_t num_slots) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
     void* fn = nullptr;
@@ -692,7 +702,7 @@ static cudaError_t make_kv_tensor_map(CUtensorMap* map, const uint8_t* kv, int H
     if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
     encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
-  const cuuint64_t dims[3] = {kSlotBytes / 4, (cuuint64_t)Hk, (cuuint64_t)num_blocks * kPage};
+  const cuuint64_t dims[3] = {kSlotBytes / 4, (cuuint64_t)Hk, (cuuint64_t)num_slots};
   const cuuint64_t strides[2] = {kSlotBytes, (cuuint64_t)Hk * kSlotBytes};
   const cuuint32_t box[3] = {kSlotBytes / 4, 1, kPage};
   const cuuint32_t elem[3] = {1, 1, 1};
@@ -703,7 +713,7 @@ static cudaError_t make_kv_tensor_map(CUtensorMap* map, const uint8_t* kv, int H
 }
 
 // Plan, then stage 1 (bracketed by the caller's timing events, if any).
-template <int NT>
+template <int NT, bool GEN>
 static cudaError_t launch_plan_and_stage1(const uint16_t* query, int64_t q_ss, int64_t q_sh,
                                           const uint8_t* kv, const int32_t* bt, const SeqRows& sl,
                                           float scale, int B, int Hq, int Hk, int num_blocks,
@@ -713,15 +723,16 @@ static cudaError_t launch_plan_and_stage1(const uint16_t* query, int64_t q_ss, i
   constexpr int NWARPS = 4, NSTAGE = kStage1Stages;
   using Lay = Stage1Layout<NT, NWARPS, NSTAGE>;
   int grid = 0;
-  cudaError_t e = stage1_grid<NT>(&grid);
+  cudaError_t e = stage1_grid<NT, GEN>(&grid);
   if (e != cudaSuccess) return e;
   CUtensorMap kv_map;
-  if ((e = make_kv_tensor_map(&kv_map, kv, Hk, num_blocks)) != cudaSuccess) return e;
-  decode_plan<<<1, kPlanThreads, 0, stream>>>(sl, B, Hk, S, max_blocks, grid * kUnitsPerCta, ws);
+  const int64_t num_slots = (int64_t)num_blocks << (4 + sl.lg_tpp);
+  if ((e = make_kv_tensor_map(&kv_map, kv, Hk, num_slots)) != cudaSuccess) return e;
+  decode_plan<<<1, kPlanThreads, 0, stream>>>(sl, B, Hk, S, grid * kUnitsPerCta, ws);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (ev_before && (e = record_timing_event(ev_before, stream)) != cudaSuccess) return e;
-  decode_stage1<NT, NWARPS, NSTAGE><<<grid, NWARPS * 32, Lay::kBytes, stream>>>(
-      query, q_ss, q_sh, kv_map, bt, sl, scale * kLog2e, Hq, Hk, Hq / Hk, num_blocks, max_blocks, S,
+  decode_stage1<NT, NWARPS, NSTAGE, GEN><<<grid, NWARPS * 32, Lay::kBytes, stream>>>(
+      query, q_ss, q_sh, kv_map, bt, sl, scale * kLog2e, Hq, Hk, Hq / Hk, num_blocks, S,
       ws, err);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (ev_after && (e = record_timing_event(ev_after, stream)) != cudaSuccess) return e;
@@ -736,12 +747,19 @@ cudaError_t launch_decode(const uint16_t* query, int64_t q_ss, int64_t q_sh, con
                           void* workspace, uint16_t* out, unsigned* err, cudaStream_t stream,
                           cudaEvent_t ev_before_stage1, cudaEvent_t ev_after_stage1) {
   const Workspace ws = workspace_layout(workspace, B, Hq, S);
-  cudaError_t e =
-      (Hq / Hk == 16)
-          ? launch_plan_and_stage1<2>(query, q_ss, q_sh, kv, bt, sl, scale, B, Hq, Hk, num_blocks,
-                                      max_blocks, S, ws, err, stream, ev_before_stage1, ev_after_stage1)
-          : launch_plan_and_stage1<1>(query, q_ss, q_sh, kv, bt, sl, scale, B, Hq, Hk, num_blocks,
-                                      max_blocks, S, ws, err, stream, ev_before_stage1, ev_after_stage1);
+  const bool gen = sl.window > 0 || sl.lg_tpp > 0;
+  const bool wide = Hq / Hk == 16;
+  auto run = [&](auto nt, auto g) {
+    return launch_plan_and_stage1<decltype(nt)::value, decltype(g)::value>(
+        query, q_ss, q_sh, kv, bt, sl, scale, B, Hq, Hk, num_blocks, max_blocks, S, ws, err, stream,
+        ev_before_stage1, ev_after_stage1);
+  };
+  using One = std::integral_constant<int, 1>;
+  using Two = std::integral_constant<int, 2>;
+  using Gen = std::true_type;
+  using Plain = std::false_type;
+  cudaError_t e = wide ? (gen ? run(Two{}, Gen{}) : run(Two{}, Plain{}))
+                       : (gen ? run(One{}, Gen{}) : run(One{}, Plain{}));
   if (e != cudaSuccess) return e;
   const int rows = B * Hq;
   decode_stage2<<<(rows + 3) / 4, 128, 0, stream>>>(ws, B, Hq, S, sinks, out);

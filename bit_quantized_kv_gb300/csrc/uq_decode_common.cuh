@@ -10,8 +10,8 @@
 
 namespace uq {
 
-constexpr int kPage = 16;                        // tokens per page (block_size)
-constexpr int kTileBytes = kPage * kSlotBytes;   // 4352 bytes per (page, kv head)
+constexpr int kPage = 16;                        // tokens per tile (the smallest block_size)
+constexpr int kTileBytes = kPage * kSlotBytes;   // 4352 bytes per (tile, kv head)
 #ifndef UQ_MIN_PAGES_PER_UNIT
 #define UQ_MIN_PAGES_PER_UNIT 8
 #endif
@@ -82,15 +82,20 @@ __device__ __forceinline__ int clamp_len(int L, int max_blocks) {
 // and every row the same pages (bt_stride = 0), as the synthetic lengths
 // arange(cached + 1, L + 1) and expanded block table of a continuation chunk.
 // A sliding window (window > 0) keeps the last `window` tokens of each row.
+// The kernels walk rows in 16-token tiles; a cache page of block_size tokens
+// holds 2^lg_tpp tiles, and a row can hold at most cap_tiles tiles (the
+// block-table width times the tiles per page).
 struct SeqRows {
   const int32_t* seq_lens;
   int64_t bt_stride;
   int mq_base;
   int window;
+  int lg_tpp;
+  int cap_tiles;
 };
 
-__device__ __forceinline__ int row_len(const SeqRows& r, int b, int max_blocks) {
-  return clamp_len(r.mq_base >= 0 ? r.mq_base + b + 1 : r.seq_lens[b], max_blocks);
+__device__ __forceinline__ int row_len(const SeqRows& r, int b) {
+  return clamp_len(r.mq_base >= 0 ? r.mq_base + b + 1 : r.seq_lens[b], r.cap_tiles);
 }
 
 // First token a row of length L attends to.
@@ -98,9 +103,9 @@ __device__ __forceinline__ int row_lo(const SeqRows& r, int L) {
   return (r.window > 0 && L > r.window) ? L - r.window : 0;
 }
 
-// Pages a row reads: [row_lo / kPage, ceil(L / kPage)).
-__device__ __forceinline__ int row_pages(const SeqRows& r, int b, int max_blocks) {
-  const int L = row_len(r, b, max_blocks);
+// Tiles a row reads: [row_lo / kPage, ceil(L / kPage)).
+__device__ __forceinline__ int row_pages(const SeqRows& r, int b) {
+  const int L = row_len(r, b);
   return (L + kPage - 1) / kPage - row_lo(r, L) / kPage;
 }
 

@@ -5,8 +5,9 @@
 // the dense prefill of a large continuation chunk).
 //
 // The kernel streams: 272 bytes read and 1024 bytes written per (token, kv
-// head).  A CTA expands one (page, kv head) tile; each of its 8 warps takes
-// two of the page's 16 tokens, and for a token lane l converts elements
+// head).  A CTA expands one (16-token tile, kv head); a page of block_size
+// tokens is block_size / 16 tiles.  Each of the 8 warps takes two of the
+// tile's 16 tokens, and for a token lane l converts elements
 // 8l .. 8l+7 of K and of V: it reads one 32-bit word of codes from each code
 // region (the warp reads each 128-byte region whole) and the scale byte of
 // block l/4, and writes 16 bytes of each output row (the warp writes each
@@ -66,19 +67,19 @@ __device__ __forceinline__ uint32_t ldg_nc_u8(const void* p) {
 
 __global__ void __launch_bounds__(kDqWarps * 32)
 full_dequant_kernel(const uint8_t* __restrict__ kv, const int32_t* __restrict__ block_table,
-                    int n_pages, int Hk, int num_blocks, uint16_t* __restrict__ k_out,
+                    int n_tiles, int lg_tpp, int Hk, int num_blocks, uint16_t* __restrict__ k_out,
                     uint16_t* __restrict__ v_out, unsigned* __restrict__ err) {
-  const int64_t tile = blockIdx.x;                  // < n_pages * Hk
-  const int p = (int)(tile / Hk), h = (int)(tile - (int64_t)p * Hk);
+  const int64_t item = blockIdx.x;                  // < n_tiles * Hk
+  const int p = (int)(item / Hk), h = (int)(item - (int64_t)p * Hk);   // tile p of the sequence
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pid = block_table[p];
-  const int64_t alloc_len = (int64_t)n_pages * kDqPage;
+  const int pid = block_table[p >> lg_tpp];
+  const int64_t alloc_len = (int64_t)n_tiles * kDqPage;
   const int64_t row0 = (int64_t)h * alloc_len + (int64_t)p * kDqPage + 2 * warp;
   uint4* ko = reinterpret_cast<uint4*>(k_out + row0 * kHeadDim) + lane;
   uint4* vo = reinterpret_cast<uint4*>(v_out + row0 * kHeadDim) + lane;
   constexpr int kRowVec = kHeadDim / 8;             // uint4 per output row
   if ((unsigned)pid >= (unsigned)num_blocks) {
-    if (threadIdx.x == 0) atomicOr(err, kErrBadPage);
+    if (threadIdx.x == 0) atomicOr(err, kErrBadPage);   // once per tile of the page
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
     ko[0] = z;
     ko[kRowVec] = z;
@@ -86,7 +87,8 @@ full_dequant_kernel(const uint8_t* __restrict__ kv, const int32_t* __restrict__ 
     vo[kRowVec] = z;
     return;
   }
-  const uint8_t* s0 = kv + (((int64_t)pid * kDqPage + 2 * warp) * Hk + h) * kSlotBytes;
+  const int64_t slot0 = ((int64_t)pid << (4 + lg_tpp)) + ((p & ((1 << lg_tpp) - 1)) << 4) + 2 * warp;
+  const uint8_t* s0 = kv + (slot0 * Hk + h) * kSlotBytes;
   const uint8_t* s1 = s0 + (int64_t)Hk * kSlotBytes;   // the next token of the page
   const uint32_t k0 = ldg_nc_32(s0 + 4 * lane), v0 = ldg_nc_32(s0 + kVCodeOff + 4 * lane);
   const uint32_t k1 = ldg_nc_32(s1 + 4 * lane), v1 = ldg_nc_32(s1 + kVCodeOff + 4 * lane);
@@ -98,13 +100,14 @@ full_dequant_kernel(const uint8_t* __restrict__ kv, const int32_t* __restrict__ 
   vo[kRowVec] = dequant_word8(v1, vb1);
 }
 
-cudaError_t launch_full_dequant(const uint8_t* kv, const int32_t* block_table, int n_pages, int Hk,
-                                int num_blocks, uint16_t* k_out, uint16_t* v_out, unsigned* err,
-                                cudaStream_t stream) {
-  const int64_t tiles = (int64_t)n_pages * Hk;
-  if (tiles <= 0) return cudaSuccess;
-  full_dequant_kernel<<<(unsigned)tiles, kDqWarps * 32, 0, stream>>>(kv, block_table, n_pages, Hk,
-                                                                    num_blocks, k_out, v_out, err);
+cudaError_t launch_full_dequant(const uint8_t* kv, const int32_t* block_table, int n_pages,
+                                int lg_tpp, int Hk, int num_blocks, uint16_t* k_out, uint16_t* v_out,
+                                unsigned* err, cudaStream_t stream) {
+  const int n_tiles = n_pages << lg_tpp;
+  const int64_t items = (int64_t)n_tiles * Hk;
+  if (items <= 0) return cudaSuccess;
+  full_dequant_kernel<<<(unsigned)items, kDqWarps * 32, 0, stream>>>(kv, block_table, n_tiles, lg_tpp,
+                                                                    Hk, num_blocks, k_out, v_out, err);
   return cudaGetLastError();
 }
 

@@ -74,10 +74,10 @@ def _pages(seq_lens: np.ndarray, bs: int) -> np.ndarray:
 def make_decode_workload(name: str, B: int, Hq: int, Hk: int, seq_lens: np.ndarray,
                          max_blocks: int, splits: int, seed: int, scale: float = 1.0 / 16,
                          outliers: bool = False, graph_replay: bool = False,
-                         spare_blocks: int = 0) -> DecodeWorkload:
+                         spare_blocks: int = 0, block_size: int = BLOCK_SIZE) -> DecodeWorkload:
     rng = np.random.default_rng(seed + 7919)
     seq_lens = np.asarray(seq_lens, dtype=np.int32)
-    pages = _pages(seq_lens, BLOCK_SIZE)
+    pages = _pages(seq_lens, block_size)
     assert int(pages.max(initial=0)) <= max_blocks
     num_blocks = int(pages.sum()) + spare_blocks
     perm = rng.permutation(max(num_blocks, 1)).astype(np.int32)
@@ -92,7 +92,7 @@ def make_decode_workload(name: str, B: int, Hq: int, Hk: int, seq_lens: np.ndarr
         crng = np.random.default_rng(seed + 104729)
         oc = np.stack([crng.choice(HEAD_DIM, 4, replace=False) for _ in range(Hk)])
     return DecodeWorkload(name, B, Hq, Hk, splits, scale, seed, seq_lens, max_blocks, bt,
-                          max(num_blocks, 1), oc, graph_replay=graph_replay)
+                          max(num_blocks, 1), oc, graph_replay=graph_replay, block_size=block_size)
 
 
 def decode_workload(name: str) -> DecodeWorkload:

@@ -28,8 +28,10 @@
  *     [0, num_blocks), a slot beyond the cache) never fault: the affected
  *     token is skipped and a bit is set in a device error word that
  *     uq_check_device_error() reads.
- *   - Supported shapes: head_dim D = 256, block_size 16, query heads per KV
- *     head (Hq / Hk) in {6, 8, 16}; other values return UQ_ERR_UNSUPPORTED.
+ *   - Supported shapes: head_dim D = 256, query heads per KV head (Hq / Hk)
+ *     in {6, 8, 16}, block_size in {16, 32, 64, 128, 256} for decode and
+ *     dequantisation (any block_size >= 1 for the store); other values
+ *     return UQ_ERR_UNSUPPORTED.  Kernels walk pages in 16-token tiles.
  *
  * Cache layout (the pages give only kv_cache's shape, (num_blocks,
  * block_size, Hk, slot_size) uint8; the byte layout below is this library's)
@@ -253,8 +255,8 @@ uq_status uq_decode_multi_query(const void *query, const void *kv_cache,
  * significant bits; a product beyond bf16's range becomes +-inf, which the
  * store never produces).  A page id outside [0, num_blocks) writes zero rows
  * and sets UQ_DEVERR_BAD_PAGE.  n_pages == 0 is a no-op.  Supported:
- * head_dim 256, block_size 16, 1 <= Hk <= 256, n_pages * block_size < 2^31
- * and n_pages * Hk < 2^31.
+ * head_dim 256, block_size in {16, 32, 64, 128, 256}, 1 <= Hk <= 256,
+ * n_pages * block_size < 2^31 and n_pages * (block_size / 16) * Hk < 2^31.
  */
 uq_status uq_full_dequant(const void *kv_cache, const int32_t *block_table, int n_pages,
                           void *k_out, void *v_out, int Hk, int head_dim, int num_blocks,

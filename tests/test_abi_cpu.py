@@ -65,7 +65,8 @@ def _decode(lib, **kw):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(D=128), binding.UQ_ERR_UNSUPPORTED),
-    (dict(bs=32), binding.UQ_ERR_UNSUPPORTED),
+    (dict(bs=24), binding.UQ_ERR_UNSUPPORTED),
+    (dict(bs=512), binding.UQ_ERR_UNSUPPORTED),
     (dict(Hq=4), binding.UQ_ERR_UNSUPPORTED),            # GQA 4
     (dict(Hq=12, Hk=1, qss=12 * 256), binding.UQ_ERR_UNSUPPORTED),
     (dict(Hq=9, Hk=2), binding.UQ_ERR_INVALID_ARG),      # not a multiple
@@ -172,7 +173,7 @@ def _dequant(lib, **kw):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(D=128), binding.UQ_ERR_UNSUPPORTED),
-    (dict(bs=32), binding.UQ_ERR_UNSUPPORTED),
+    (dict(bs=48), binding.UQ_ERR_UNSUPPORTED),
     (dict(Hk=0), binding.UQ_ERR_UNSUPPORTED),
     (dict(Hk=300), binding.UQ_ERR_UNSUPPORTED),
     (dict(sb=288), binding.UQ_ERR_INVALID_ARG),
