@@ -7,9 +7,13 @@
 // Three kernels on the caller's stream:
 //
 // Plan (one CTA).  Reads seq_lens and chooses, for the whole batch, one unit
-// size T (pages of one kv head) so that the batch splits into about
-// kUnitsPerCta work units per resident stage-1 CTA, never below
-// kMinPagesPerUnit pages.  Sequence b gets n_b = min(S, ceil(P_b / T)) splits
+// size T (pages of one kv head) so that the batch splits into U work units
+// per resident stage-1 CTA, never below kMinPagesPerUnit pages.  Each unit
+// costs a fixed start (first copies in flight, query prologue, merge and
+// partial write) while the last units decide the tail, which grows with
+// the unit size; the sum is smallest near U = sqrt(work per CTA / 2 fixed
+// cost), which with the measured costs is U = sqrt(tiles per CTA / 64),
+// kept in [2, 8].  Sequence b gets n_b = min(S, ceil(P_b / T)) splits
 // of whole pages.  Units (sequence, split, kv head) are listed with the
 // longest units first; the plan also resets the unit counter.
 //
@@ -51,7 +55,7 @@ namespace uq {
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kPlanThreads)
 decode_plan(const SeqRows rows, int B, int Hk, int S,
-            int target_units, Workspace ws) {
+            int grid, Workspace ws) {
   __shared__ long long s_part[kPlanThreads / 32];
   __shared__ int s_hist[32], s_cursor[32], s_wsum[kPlanThreads / 32];
   __shared__ long long s_total;
@@ -72,7 +76,10 @@ decode_plan(const SeqRows rows, int B, int Hk, int S,
   }
   __syncthreads();
   const long long work = s_total * Hk;
-  long long T = (work + target_units - 1) / max(target_units, 1);
+  const float per_cta = (float)work / (float)max(grid, 1);
+  const int upc = min(kMaxUnitsPerCta, max(kMinUnitsPerCta, (int)sqrtf(per_cta / kUnitCostTiles)));
+  const long long target_units = (long long)grid * upc;
+  long long T = (work + target_units - 1) / target_units;
   if (T < kMinPagesPerUnit) T = kMinPagesPerUnit;
 
   for (int b = tid; b < B; b += kPlanThreads) {
@@ -728,7 +735,7 @@ static cudaError_t launch_plan_and_stage1(const uint16_t* query, int64_t q_ss, i
   CUtensorMap kv_map;
   const int64_t num_slots = (int64_t)num_blocks << (4 + sl.lg_tpp);
   if ((e = make_kv_tensor_map(&kv_map, kv, Hk, num_slots)) != cudaSuccess) return e;
-  decode_plan<<<1, kPlanThreads, 0, stream>>>(sl, B, Hk, S, grid * kUnitsPerCta, ws);
+  decode_plan<<<1, kPlanThreads, 0, stream>>>(sl, B, Hk, S, grid, ws);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (ev_before && (e = record_timing_event(ev_before, stream)) != cudaSuccess) return e;
   decode_stage1<NT, NWARPS, NSTAGE, GEN><<<grid, NWARPS * 32, Lay::kBytes, stream>>>(

@@ -15,8 +15,8 @@ constexpr int kTileBytes = kPage * kSlotBytes;   // 4352 bytes per (tile, kv hea
 #ifndef UQ_MIN_PAGES_PER_UNIT
 #define UQ_MIN_PAGES_PER_UNIT 8
 #endif
-#ifndef UQ_UNITS_PER_CTA
-#define UQ_UNITS_PER_CTA 4
+#ifndef UQ_UNIT_COST_TILES
+#define UQ_UNIT_COST_TILES 64
 #endif
 #ifndef UQ_S1_NSTAGE
 #define UQ_S1_NSTAGE 2
@@ -25,7 +25,8 @@ constexpr int kTileBytes = kPage * kSlotBytes;   // 4352 bytes per (tile, kv hea
 #define UQ_S1_MIN_BLOCKS 4
 #endif
 constexpr int kMinPagesPerUnit = UQ_MIN_PAGES_PER_UNIT;  // floor of 128 tokens per split
-constexpr int kUnitsPerCta = UQ_UNITS_PER_CTA;           // work units per resident CTA
+constexpr float kUnitCostTiles = UQ_UNIT_COST_TILES;     // work units per CTA = sqrt(tiles / this)
+constexpr int kMinUnitsPerCta = 2, kMaxUnitsPerCta = 8;
 constexpr int kStage1Stages = UQ_S1_NSTAGE;              // pages in flight per warp
 constexpr int kPlanThreads = 1024;
 constexpr float kLog2e = 1.4426950408889634f;
