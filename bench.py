@@ -720,8 +720,8 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="outlier_long",
-                    choices=["tiny", "batch", "outlier_long", "skewed", "outlier_ncu", "store",
-                             "dequant", "mq"])
+                    choices=["tiny", "batch", "outlier_long", "skewed", "outlier_ncu", "skewed_ncu",
+                             "store", "dequant", "mq"])
     ap.add_argument("--impl", default="uq", choices=["uq", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the CPU baseline")

@@ -106,6 +106,8 @@ def decode_workload(name: str) -> DecodeWorkload:
                   max_model_len 131072, S=32, seed 3, CUDA-graph replay
     outlier_ncu   B=16, Hq=48, Hk=8, L=16384 each, outlier K: the outlier shape at a
                   size a full ncu capture can replay (570 MB of cache)
+    skewed_ncu    B=16, Hq=64, Hk=4 (GQA 16), L=16384 each: the skewed head shape
+                  for a full ncu capture (285 MB of cache)
     All use D=256, block_size=16, scale=1/16, bf16 q/K/V ~ N(0,1).
     """
     if name == "tiny":
@@ -124,6 +126,11 @@ def decode_workload(name: str) -> DecodeWorkload:
         # of cache, above L2, small enough for a full ncu capture)
         return make_decode_workload("outlier_ncu", 16, 48, 8, np.full(16, 16384), 16384 // BLOCK_SIZE,
                                     32, seed=2, outliers=True)
+    if name == "skewed_ncu":
+        # the skewed workload's GQA-16 head shape at 16 sequences of 16384
+        # tokens (285 MB of cache, above L2, small enough for a full ncu capture)
+        return make_decode_workload("skewed_ncu", 16, 64, 4, np.full(16, 16384), 16384 // BLOCK_SIZE,
+                                    32, seed=3)
     if name == "skewed":
         rng = np.random.default_rng(3)
         lens = np.floor(np.exp(rng.uniform(math.log(128), math.log(131072), size=128)))
@@ -133,7 +140,7 @@ def decode_workload(name: str) -> DecodeWorkload:
     raise KeyError(name)
 
 
-DECODE_WORKLOADS = ("tiny", "batch", "outlier_long", "skewed", "outlier_ncu")
+DECODE_WORKLOADS = ("tiny", "batch", "outlier_long", "skewed", "outlier_ncu", "skewed_ncu")
 
 
 def _gen(device, seed: int) -> torch.Generator:
