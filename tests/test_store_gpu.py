@@ -163,3 +163,22 @@ def test_store_full_size_bit_exact():
     ref = _oracle_store(k, v, slots, shape)
     n_bad = int(np.count_nonzero(got != ref))
     assert n_bad == 0, f"{n_bad} of {got.size} bytes differ"
+
+
+@pytest.mark.parametrize("Hk", [1, 3])
+def test_store_bf16_special_values_bit_exact(Hk):
+    """bf16 K and V built from the special fp32 rows (ties, saturation,
+    signed zeros, subnormal blocks, huge exponents): V reaches the quantiser
+    unrotated, K after the butterfly, both through the bf16 path's lane
+    layout."""
+    n_rows = 48
+    kr = _special_rows(n_rows * Hk, 41)
+    kr[4::8] *= np.float32(1e-3)   # keep the butterfly's sums of the huge rows finite
+    k = torch.from_numpy(kr).to(torch.bfloat16).view(n_rows, Hk, 256)
+    v = torch.from_numpy(_special_rows(n_rows * Hk, 42)[::-1].copy()).to(torch.bfloat16).view(n_rows, Hk, 256)
+    slots = torch.from_numpy(np.random.default_rng(43).permutation(64)[:n_rows].astype(np.int64))
+    shape = (4, 16, Hk, 272)
+    cache = torch.zeros(shape, dtype=torch.uint8, device="cuda")
+    binding.uq_store(k.cuda(), v.cuda(), cache, slots.cuda())
+    assert binding.uq_check_device_error() == 0
+    assert np.array_equal(cache.cpu().numpy(), _oracle_store(k, v, slots, shape))
