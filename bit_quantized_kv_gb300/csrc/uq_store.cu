@@ -19,7 +19,7 @@
 // takes two shuffles.  Each lane writes the 8 codes of each register group
 // as one 4-byte word (bytes 32i + 4g of the code array).
 //
-// fp32 pre-rotated path (store_kernel): lane g owns elements [32g, 32g+32),
+// fp32 pre-rotated path (store_rotated_f32_kernel): lane g owns elements [32g, 32g+32),
 // exactly the g-th UE8M0 block, and writes 16 code bytes at once.
 #include "uq_device.cuh"
 
