@@ -422,9 +422,12 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
         const int first = lo - page * kPage;   // window start within this page
         const bool v0 = gq < nvalid && (!GEN || gq >= first);
         const bool v1 = gq + 8 < nvalid && (!GEN || gq + 8 >= first);
-        uint32_t pw[NT][2];
-        bool rescale = false;
-        float mu_prev[NT][2];
+        // A lane's own scores decide whether any running maximum can move
+        // this page; only then are the row maxima reduced across the 8 lanes
+        // of a row.  Otherwise every maximum stays where it is, which is what
+        // the reduction would have decided too.
+        float sv[NT][2][2], uv[NT][2][2];   // [tile][row half][token gq, gq + 8]
+        bool grow = false;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           float sres[4];
@@ -435,30 +438,51 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
             for (int ch = 1; ch < NCH; ++ch) acc += sacc[nt][ch][k];
             sres[k] = acc;
           }
-          float w4[4];
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const float s0 = v0 ? sres[h] * fk0 : -INFINITY;
             const float s1 = v1 ? sres[2 + h] * fk1 : -INFINITY;
-            const float u0 = s0 + evf0;
-            const float u1 = s1 + evf1;
-            float tmax = fmaxf(s0, s1), umax = fmaxf(u0, u1);
+            sv[nt][h][0] = s0;
+            sv[nt][h][1] = s1;
+            uv[nt][h][0] = s0 + evf0;
+            uv[nt][h][1] = s1 + evf1;
+            grow |= fmaxf(s0, s1) > m_run[nt][h] + kLazyMaxLog2;
+            grow |= fmaxf(uv[nt][h][0], uv[nt][h][1]) > mu_run[nt][h] + kLazyMaxLog2;
+          }
+        }
+        bool rescale = false;
+        float mu_prev[NT][2];
+        if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll
-            for (int msk = 4; msk < 32; msk <<= 1) {
-              tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, msk));
-              umax = fmaxf(umax, __shfl_xor_sync(0xffffffffu, umax, msk));
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              float tmax = fmaxf(sv[nt][h][0], sv[nt][h][1]);
+              float umax = fmaxf(uv[nt][h][0], uv[nt][h][1]);
+#pragma unroll
+              for (int msk = 4; msk < 32; msk <<= 1) {
+                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, msk));
+                umax = fmaxf(umax, __shfl_xor_sync(0xffffffffu, umax, msk));
+              }
+              const float m_old = m_run[nt][h], mu_old = mu_run[nt][h];
+              const float m_new = tmax > m_old + kLazyMaxLog2 ? tmax : m_old;
+              const float mu_new = umax > mu_old + kLazyMaxLog2 ? umax : mu_old;
+              l_run[nt][h] *= fast_exp2(m_old - m_new);
+              mu_prev[nt][h] = mu_old;
+              rescale |= mu_new != mu_old;
+              m_run[nt][h] = m_new;
+              mu_run[nt][h] = mu_new;
             }
-            const float m_old = m_run[nt][h], mu_old = mu_run[nt][h];
-            const float m_new = tmax > m_old + kLazyMaxLog2 ? tmax : m_old;
-            const float mu_new = umax > mu_old + kLazyMaxLog2 ? umax : mu_old;
-            l_run[nt][h] = l_run[nt][h] * fast_exp2(m_old - m_new) + fast_exp2(s0 - m_new) +
-                           fast_exp2(s1 - m_new);
-            mu_prev[nt][h] = mu_old;
-            rescale |= mu_new != mu_old;
-            m_run[nt][h] = m_new;
-            mu_run[nt][h] = mu_new;
-            w4[h] = fast_exp2(u0 - mu_new);
-            w4[2 + h] = fast_exp2(u1 - mu_new);
+        }
+        uint32_t pw[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          float w4[4];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            l_run[nt][h] += fast_exp2(sv[nt][h][0] - m_run[nt][h]) + fast_exp2(sv[nt][h][1] - m_run[nt][h]);
+            w4[h] = fast_exp2(uv[nt][h][0] - mu_run[nt][h]);
+            w4[2 + h] = fast_exp2(uv[nt][h][1] - mu_run[nt][h]);
           }
           pw[nt][0] = movmatrix_trans(pack_f16x2(w4[0], w4[1]));
           pw[nt][1] = movmatrix_trans(pack_f16x2(w4[2], w4[3]));
