@@ -56,6 +56,7 @@ def _peaks():
 
 
 DEQUANT_SOURCES = ["bit_quantized_kv_gb300/csrc/uq_dequant.cu", "bit_quantized_kv_gb300/csrc/uq_device.cuh"]
+STORE_SOURCES = ["bit_quantized_kv_gb300/csrc/uq_store.cu", "bit_quantized_kv_gb300/csrc/uq_device.cuh"]
 
 
 def _source_hash(sources=None) -> str:
@@ -82,10 +83,12 @@ def _traffic_from_profile(workload: str, profile: str | None = None, sources=Non
             vals[k.strip()] = v.strip().strip("`")
     if vals.get("source_sha256_16") != _source_hash(sources):
         return None
-    try:
-        return float(vals["dram_bytes_per_launch_full_size"])
-    except (KeyError, ValueError):
-        return None
+    for key in ("dram_bytes_per_launch_full_size", "dram_bytes_per_launch"):
+        try:
+            return float(vals[key])
+        except (KeyError, ValueError):
+            continue
+    return None
 
 
 class ClockSampler:
@@ -414,7 +417,8 @@ def run_gpu_store(args, rank, local, world, dev, stream, peak, peak_kind):
                        "bytes_per_step": by, "l2": "inputs larger than L2"},
             "roofline": {"bound": "hbm", "kernel": "store", "achieved": round(ach, 2), "peak": peak,
                          "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
-                         "frac": round(ach / peak, 4), "traffic": None},
+                         "frac": round(ach / peak, 4),
+                         "traffic": _traffic_from_profile("store", "store_kernel_store.md", STORE_SOURCES)},
             "gpu_launches": args.steps, "clocks": clocks.summary()}
 
 
