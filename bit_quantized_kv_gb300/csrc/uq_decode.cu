@@ -42,6 +42,14 @@
 // lane (g = lane/4, c = lane%4) owns head dims [64c, 64c+64) of K (k-step i
 // covers 64c + 4i .. +3) and V head dims [32g, 32g+32) (one UE8M0 block).
 //
+// 16-row query groups (GQA 16) keep O^T in tensor memory instead of
+// registers: 128 fp32 per lane would hold a thread above 168 registers and
+// the SM at 8 warps.  Each CTA allocates 128 TMEM columns over its 128
+// lanes; warp w works in lanes 32w .. 32w+31 only, as per-thread storage.
+// PV loads the 32 columns of one V word (both 8-row tiles), runs its MMAs
+// and stores them back; the rare rescale and the final merge go through the
+// same columns.  At 168 registers three CTAs (12 warps) fit per SM.
+//
 // Stage 2: one warp per (sequence, query head) merges the active splits with
 // the log-sum-exp rule and writes bf16.
 #include <type_traits>
@@ -153,8 +161,12 @@ decode_plan(const SeqRows rows, int B, int Hk, int S,
 template <int NT, int NWARPS, int NSTAGE>
 struct Stage1Layout {
   static constexpr int kRows = NT * 8;                       // padded query rows
+  // 16-row groups keep O^T in tensor memory between pages (see kTmemCols)
+  static constexpr bool kTmemO = NT == 2;
   static constexpr int kStageBytes = NWARPS * NSTAGE * kTileBytes;
-  static constexpr int kORowStride = kHeadDim + 4;           // floats
+  static constexpr int kMergeParts = kTmemO ? 2 : 1;         // head-dim parts merged in turn
+  static constexpr int kPartDims = kHeadDim / kMergeParts;
+  static constexpr int kORowStride = kPartDims + 4;          // floats
   static constexpr int kMergeBytes = NWARPS * kRows * kORowStride * 4;
   static constexpr int kUnionBytes = kStageBytes > kMergeBytes ? kStageBytes : kMergeBytes;
   static constexpr int kStatsOff = kUnionBytes;              // [NWARPS][kRows][4] floats
@@ -169,7 +181,7 @@ struct Stage1Layout {
   static constexpr int kMetaOff = kLutOff + kLutBytes;
   static constexpr int kBarOff = kMetaOff + NWARPS * kMetaWarpBytes;
   static constexpr int kBarBytes = NWARPS * NSTAGE * 8;
-  static constexpr int kMiscOff = kBarOff + kBarBytes;       // unit id, abort flag
+  static constexpr int kMiscOff = kBarOff + kBarBytes;       // unit id, abort flag, TMEM base
   static constexpr int kQOff = (kMiscOff + 16 + 127) / 128 * 128;
   static constexpr int kQRowBytes = kHeadDim * 2 + 16;       // padded: conflict-free ldmatrix
   static constexpr int kQBytes = kRows * kQRowBytes;
@@ -179,7 +191,7 @@ struct Stage1Layout {
 // GEN: a sliding window or pages of more than 16 tokens.  The plain
 // instantiation (block_size 16, no window) folds both away.
 template <int NT, int NWARPS, int NSTAGE, bool GEN>
-__global__ void __launch_bounds__(NWARPS * 32, NT == 1 ? UQ_S1_MIN_BLOCKS : 2)
+__global__ void __launch_bounds__(NWARPS * 32, NT == 1 ? UQ_S1_MIN_BLOCKS : kTmemCtasPerSm)
 decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
               const __grid_constant__ CUtensorMap kv_map, const int32_t* __restrict__ block_table,
               const SeqRows rows, float scale_log2e, int Hq, int Hk,
@@ -208,7 +220,18 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
     const uint32_t h = pow2_neg_f16(i);
     reinterpret_cast<uint32_t*>(smem + Lay::kLutOff)[i] = h | (h << 16);
   }
+  if constexpr (Lay::kTmemO) {
+    if (warp == 0) tmem_alloc(smem_base + Lay::kMiscOff + 8, kTmemCols);
+    tc_fence_before_sync();
+  }
   __syncthreads();
+  // this warp's O^T columns: its own 32 lanes, columns 32q + 16nt + 4e + k hold
+  // o[nt][4q + e][k]
+  uint32_t o_taddr = 0;
+  if constexpr (Lay::kTmemO) {
+    tc_fence_after_sync();
+    o_taddr = (uint32_t)s_misc[2] + ((uint32_t)(32 * warp) << 16);
+  }
 
   const int n_units = ws.hdr[0];
   uint32_t tiles_done = 0;   // this warp's tiles so far: drives stage and parity
@@ -327,6 +350,13 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int mt = 0; mt < 16; ++mt) o[nt][mt][0] = o[nt][mt][1] = o[nt][mt][2] = o[nt][mt][3] = 0.f;
+    if constexpr (Lay::kTmemO) {
+      float z[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) z[i] = 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tmem_st32(o_taddr + 32 * q, z);
+    }
     float m_run[NT][2], mu_run[NT][2], l_run[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
@@ -342,7 +372,11 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
     int stg = stg0;
     uint32_t phase = ph0;
     for (; j < n_my; ++j) {
-      if (!mbar_wait(bar_base + 8 * stg, phase)) {
+      // With O^T in tensor memory the warp gives up together, so its
+      // warp-collective tcgen05 instructions always run converged.
+      bool arrived = mbar_wait(bar_base + 8 * stg, phase);
+      if constexpr (Lay::kTmemO) arrived = __all_sync(0xffffffffu, arrived);
+      if (!arrived) {
         timed_out = true;
         break;
       }
@@ -488,16 +522,38 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
           pw[nt][1] = movmatrix_trans(pack_f16x2(w4[2], w4[3]));
         }
         if (__any_sync(0xffffffffu, rescale)) {
+          if constexpr (Lay::kTmemO) {
+            tmem_wait_st();
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            const float a0 = fast_exp2(mu_prev[nt][0] - mu_run[nt][0]);
-            const float a1 = fast_exp2(mu_prev[nt][1] - mu_run[nt][1]);
+            for (int q = 0; q < 4; ++q) {
+              float oc[32];
+              tmem_ld32(o_taddr + 32 * q, oc);
 #pragma unroll
-            for (int mt = 0; mt < 16; ++mt) {
-              o[nt][mt][0] *= a0;
-              o[nt][mt][1] *= a1;
-              o[nt][mt][2] *= a0;
-              o[nt][mt][3] *= a1;
+              for (int nt = 0; nt < NT; ++nt) {
+                const float a0 = fast_exp2(mu_prev[nt][0] - mu_run[nt][0]);
+                const float a1 = fast_exp2(mu_prev[nt][1] - mu_run[nt][1]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  oc[16 * nt + 4 * e] *= a0;
+                  oc[16 * nt + 4 * e + 1] *= a1;
+                  oc[16 * nt + 4 * e + 2] *= a0;
+                  oc[16 * nt + 4 * e + 3] *= a1;
+                }
+              }
+              tmem_st32(o_taddr + 32 * q, oc);
+            }
+          } else {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              const float a0 = fast_exp2(mu_prev[nt][0] - mu_run[nt][0]);
+              const float a1 = fast_exp2(mu_prev[nt][1] - mu_run[nt][1]);
+#pragma unroll
+              for (int mt = 0; mt < 16; ++mt) {
+                o[nt][mt][0] *= a0;
+                o[nt][mt][1] *= a1;
+                o[nt][mt][2] *= a0;
+                o[nt][mt][3] *= a1;
+              }
             }
           }
         }
@@ -509,6 +565,7 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
         const uint4 vd = lds128(sb + td * kSlotBytes + voff);
         const uint32_t vaw[4] = {va.x, va.y, va.z, va.w}, vbw[4] = {vb.x, vb.y, vb.z, vb.w};
         const uint32_t vcw[4] = {vc.x, vc.y, vc.z, vc.w}, vdw[4] = {vd.x, vd.y, vd.z, vd.w};
+        if constexpr (Lay::kTmemO) tmem_wait_st();   // the last page's O^T columns are back
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           // pair the same head dim of two tokens in one byte: (token t+1 << 4) | token t
@@ -521,13 +578,28 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
           f16x2x4_from_e2m1_word(hi01, A1);
           f16x2x4_from_e2m1_word(lo89, A2);
           f16x2x4_from_e2m1_word(hi89, A3);
+          if constexpr (Lay::kTmemO) {
+            float oc[32];
+            tmem_ld32(o_taddr + 32 * q, oc);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const uint32_t a0 = hmul2(A0[e], rv01), a1 = hmul2(A1[e], rv01);
-            const uint32_t a2 = hmul2(A2[e], rv89), a3 = hmul2(A3[e], rv89);
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t a0 = hmul2(A0[e], rv01), a1 = hmul2(A1[e], rv01);
+              const uint32_t a2 = hmul2(A2[e], rv89), a3 = hmul2(A3[e], rv89);
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-              mma_f16_16816(o[nt][4 * q + e], a0, a1, a2, a3, pw[nt][0], pw[nt][1]);
+              for (int nt = 0; nt < NT; ++nt)
+                mma_f16_16816(*reinterpret_cast<float(*)[4]>(oc + 16 * nt + 4 * e), a0, a1, a2, a3,
+                              pw[nt][0], pw[nt][1]);
+            }
+            tmem_st32(o_taddr + 32 * q, oc);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t a0 = hmul2(A0[e], rv01), a1 = hmul2(A1[e], rv01);
+              const uint32_t a2 = hmul2(A2[e], rv89), a3 = hmul2(A3[e], rv89);
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+                mma_f16_16816(o[nt][4 * q + e], a0, a1, a2, a3, pw[nt][0], pw[nt][1]);
+            }
           }
         }
       }
@@ -574,24 +646,16 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
     float* stats = reinterpret_cast<float*>(smem + Lay::kStatsOff);
     float* rowinfo = reinterpret_cast<float*>(smem + Lay::kRowInfoOff);
     float* my_o = osm + warp * Lay::kRows * Lay::kORowStride;
+    if (gq == 0) {
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int r0 = nt * 8 + 2 * c;
-#pragma unroll
-      for (int mt = 0; mt < 16; ++mt) {
-        const int d = 32 * gq + 2 * mt;
-        *reinterpret_cast<float2*>(my_o + r0 * Lay::kORowStride + d) = make_float2(o[nt][mt][0], o[nt][mt][2]);
-        *reinterpret_cast<float2*>(my_o + (r0 + 1) * Lay::kORowStride + d) = make_float2(o[nt][mt][1], o[nt][mt][3]);
-      }
-      if (gq == 0) {
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          float* st = stats + (warp * Lay::kRows + r0 + h) * 4;
+          float* st = stats + (warp * Lay::kRows + nt * 8 + 2 * c + h) * 4;
           st[0] = m_run[nt][h];
           st[1] = mu_run[nt][h];
           st[2] = l_run[nt][h];
         }
-      }
     }
     __syncthreads();
     if (threadIdx.x < QG) {
@@ -611,23 +675,70 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
       ri[NWARPS] = Ls > 0.f ? M + fast_log2(Ls) : -INFINITY;
       ws.part_lse[((int64_t)(b * Hq + g * QG + r)) * S + split] = ri[NWARPS];
     }
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < QG * (kHeadDim / 4); idx += NWARPS * 32) {
-      const int r = idx / (kHeadDim / 4), d4 = (idx % (kHeadDim / 4)) * 4;
-      const float* ri = rowinfo + r * (NWARPS + 2);
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    // Lane (gq, c) holds head dims 32gq .. 32gq+31 of rows nt*8 + 2c (+1);
+    // the head dims are merged in kMergeParts parts through one buffer.
 #pragma unroll
-      for (int w = 0; w < NWARPS; ++w) {
-        const float f = ri[w];
-        const float4 v = *reinterpret_cast<const float4*>(osm + (w * Lay::kRows + r) * Lay::kORowStride + d4);
-        acc.x += v.x * f;
-        acc.y += v.y * f;
-        acc.z += v.z * f;
-        acc.w += v.w * f;
+    for (int part = 0; part < Lay::kMergeParts; ++part) {
+      const bool mine = (32 * gq) / Lay::kPartDims == part;
+      const int dbase = 32 * gq - part * Lay::kPartDims;
+      if constexpr (Lay::kTmemO) {
+        tmem_wait_st();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float oc[32];
+          tmem_ld32(o_taddr + 32 * q, oc);
+          if (mine) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              const int r0 = nt * 8 + 2 * c;
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float* v = oc + 16 * nt + 4 * e;
+                const int d = dbase + 2 * (4 * q + e);
+                *reinterpret_cast<float2*>(my_o + r0 * Lay::kORowStride + d) = make_float2(v[0], v[2]);
+                *reinterpret_cast<float2*>(my_o + (r0 + 1) * Lay::kORowStride + d) = make_float2(v[1], v[3]);
+              }
+            }
+          }
+        }
+      } else if (mine) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int r0 = nt * 8 + 2 * c;
+#pragma unroll
+          for (int mt = 0; mt < 16; ++mt) {
+            const int d = dbase + 2 * mt;
+            *reinterpret_cast<float2*>(my_o + r0 * Lay::kORowStride + d) = make_float2(o[nt][mt][0], o[nt][mt][2]);
+            *reinterpret_cast<float2*>(my_o + (r0 + 1) * Lay::kORowStride + d) = make_float2(o[nt][mt][1], o[nt][mt][3]);
+          }
+        }
       }
-      *reinterpret_cast<float4*>(ws.part_o + (((int64_t)(b * Hq + g * QG + r)) * S + split) * kHeadDim + d4) = acc;
+      __syncthreads();
+      for (int idx = threadIdx.x; idx < QG * (Lay::kPartDims / 4); idx += NWARPS * 32) {
+        const int r = idx / (Lay::kPartDims / 4), d4 = (idx % (Lay::kPartDims / 4)) * 4;
+        const float* ri = rowinfo + r * (NWARPS + 2);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < NWARPS; ++w) {
+          const float f = ri[w];
+          const float4 v = *reinterpret_cast<const float4*>(osm + (w * Lay::kRows + r) * Lay::kORowStride + d4);
+          acc.x += v.x * f;
+          acc.y += v.y * f;
+          acc.z += v.z * f;
+          acc.w += v.w * f;
+        }
+        *reinterpret_cast<float4*>(ws.part_o + (((int64_t)(b * Hq + g * QG + r)) * S + split) * kHeadDim +
+                                   part * Lay::kPartDims + d4) = acc;
+      }
+      __syncthreads();  // the merge buffer (the stage buffers) and Q' are free again
     }
-    __syncthreads();  // merge buffers (stage buffers) and Q' are free again
+  }
+  if constexpr (Lay::kTmemO) {
+    tmem_wait_st();
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == 0) tmem_dealloc((uint32_t)s_misc[2], kTmemCols);
   }
 }
 
@@ -712,8 +823,27 @@ static cudaError_t stage1_grid(int* grid) {
   int sms = 0, per_sm = 0;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NWARPS * 32, Lay::kBytes);
-  if (e != cudaSuccess) return e;
+  if constexpr (Lay::kTmemO) {
+    // The occupancy query does not model a kernel that allocates tensor
+    // memory, so count the limits directly: registers per scheduler (one
+    // warp of each CTA per scheduler), shared memory, and the 512 TMEM
+    // columns of an SM.
+    cudaFuncAttributes fa;
+    int smem_sm = 0, reserved = 0;
+    if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess)
+      return e;
+    if ((e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess)
+      return e;
+    const int regs = (fa.numRegs + 7) & ~7;
+    const int by_regs = regs > 0 ? 16384 / (regs * 32) : 1;
+    const int by_smem = smem_sm / (Lay::kBytes + reserved);
+    per_sm = by_regs < by_smem ? by_regs : by_smem;
+    if (per_sm > (int)(512 / kTmemCols)) per_sm = (int)(512 / kTmemCols);
+  } else {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NWARPS * 32, Lay::kBytes);
+    if (e != cudaSuccess) return e;
+  }
   *grid = sms * (per_sm > 0 ? per_sm : 1);
   if (dev >= 0 && dev < 64) grid_of_device[dev] = *grid;
   return cudaSuccess;

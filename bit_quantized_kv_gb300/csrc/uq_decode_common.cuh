@@ -28,6 +28,14 @@ constexpr int kMinPagesPerUnit = UQ_MIN_PAGES_PER_UNIT;  // floor of 128 tokens 
 constexpr float kUnitCostTiles = UQ_UNIT_COST_TILES;     // work units per CTA = sqrt(tiles / this)
 constexpr int kMinUnitsPerCta = 2, kMaxUnitsPerCta = 8;
 constexpr int kStage1Stages = UQ_S1_NSTAGE;              // pages in flight per warp
+// 16-row query groups keep O^T (128 fp32 per lane) in tensor memory: 128
+// columns over all 128 lanes per CTA, each warp in its own 32 lanes.  That
+// frees the registers for 3 resident CTAs per SM (4 would need <= 128).
+constexpr uint32_t kTmemCols = 128;
+#ifndef UQ_S1_NT2_MIN_BLOCKS
+#define UQ_S1_NT2_MIN_BLOCKS 3
+#endif
+constexpr int kTmemCtasPerSm = UQ_S1_NT2_MIN_BLOCKS;
 constexpr int kPlanThreads = 1024;
 constexpr float kLog2e = 1.4426950408889634f;
 // A running softmax maximum (log2 units) moves only when a page's maximum
