@@ -565,7 +565,14 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
         const uint4 vd = lds128(sb + td * kSlotBytes + voff);
         const uint32_t vaw[4] = {va.x, va.y, va.z, va.w}, vbw[4] = {vb.x, vb.y, vb.z, vb.w};
         const uint32_t vcw[4] = {vc.x, vc.y, vc.z, vc.w}, vdw[4] = {vd.x, vd.y, vd.z, vd.w};
-        if constexpr (Lay::kTmemO) tmem_wait_st();   // the last page's O^T columns are back
+        // O^T half h = 2q + nt (columns 16h .. 16h+15) is loaded while the
+        // MMAs of half h-1 run; the two halves alternate between ob[0], ob[1].
+        float ob[2][16];
+        if constexpr (Lay::kTmemO) {
+          tmem_wait_st();   // the last page's O^T columns are back
+          tmem_ld16_issue(o_taddr, ob[0]);
+          tmem_ld16_wait(ob[0]);
+        }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           // pair the same head dim of two tokens in one byte: (token t+1 << 4) | token t
@@ -578,28 +585,32 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
           f16x2x4_from_e2m1_word(hi01, A1);
           f16x2x4_from_e2m1_word(lo89, A2);
           f16x2x4_from_e2m1_word(hi89, A3);
+          uint32_t a[4][4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            a[e][0] = hmul2(A0[e], rv01);
+            a[e][1] = hmul2(A1[e], rv01);
+            a[e][2] = hmul2(A2[e], rv89);
+            a[e][3] = hmul2(A3[e], rv89);
+          }
           if constexpr (Lay::kTmemO) {
-            float oc[32];
-            tmem_ld32(o_taddr + 32 * q, oc);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const uint32_t a0 = hmul2(A0[e], rv01), a1 = hmul2(A1[e], rv01);
-              const uint32_t a2 = hmul2(A2[e], rv89), a3 = hmul2(A3[e], rv89);
+            for (int nt = 0; nt < NT; ++nt) {
+              const int h = 2 * q + nt, cur = h & 1;
+              if (h < 7) tmem_ld16_issue(o_taddr + 16 * (h + 1), ob[cur ^ 1]);
 #pragma unroll
-              for (int nt = 0; nt < NT; ++nt)
-                mma_f16_16816(*reinterpret_cast<float(*)[4]>(oc + 16 * nt + 4 * e), a0, a1, a2, a3,
-                              pw[nt][0], pw[nt][1]);
+              for (int e = 0; e < 4; ++e)
+                mma_f16_16816(*reinterpret_cast<float(*)[4]>(ob[cur] + 4 * e), a[e][0], a[e][1], a[e][2],
+                              a[e][3], pw[nt][0], pw[nt][1]);
+              tmem_st16(o_taddr + 16 * h, ob[cur]);
+              if (h < 7) tmem_ld16_wait(ob[cur ^ 1]);
             }
-            tmem_st32(o_taddr + 32 * q, oc);
           } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const uint32_t a0 = hmul2(A0[e], rv01), a1 = hmul2(A1[e], rv01);
-              const uint32_t a2 = hmul2(A2[e], rv89), a3 = hmul2(A3[e], rv89);
+            for (int e = 0; e < 4; ++e)
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt)
-                mma_f16_16816(o[nt][4 * q + e], a0, a1, a2, a3, pw[nt][0], pw[nt][1]);
-            }
+                mma_f16_16816(o[nt][4 * q + e], a[e][0], a[e][1], a[e][2], a[e][3], pw[nt][0], pw[nt][1]);
           }
         }
       }
