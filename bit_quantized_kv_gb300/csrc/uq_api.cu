@@ -294,7 +294,7 @@ uq_status uq_decode_ex(const void* query, const void* kv_cache, const int32_t* b
   if (!aligned(seq_lens, 4) || (sinks && !aligned(sinks, 4)))
     return fail(UQ_ERR_INVALID_ARG, "block_table, seq_lens and sinks must be 4-byte aligned");
   const uq::SeqRows rows{seq_lens, (int64_t)max_blocks_per_seq, -1, sliding_window,
-                         log2_tiles_per_page(block_size), max_blocks_per_seq * (block_size / 16)};
+                         log2_tiles_per_page(block_size), max_blocks_per_seq * (block_size / 16), 1, B};
   return launch_checked_decode(query, kv_cache, block_table, rows, scale, sinks, max_num_kv_splits,
                                workspace, out, B, Hq, Hk, num_blocks, max_blocks_per_seq,
                                q_stride_seq, q_stride_head, stream);
@@ -328,8 +328,12 @@ uq_status uq_decode_multi_query(const void* query, const void* kv_cache, const i
     return fail(UQ_ERR_INVALID_ARG, "cached_len %d + q_len %d exceeds the %d pages of block_table",
                 cached_len, q_len, max_blocks_per_seq);
   if (sinks && !aligned(sinks, 4)) return fail(UQ_ERR_INVALID_ARG, "sinks must be 4-byte aligned");
+  // Two chunk positions share a work unit when their query rows fit one
+  // 16-row group (6 or 8 query heads per kv head): each page is read and
+  // dequantised once for both.
+  const int pack = (q_len > 1 && 2 * (Hq / Hk) <= 16) ? 2 : 1;
   const uq::SeqRows rows{nullptr, 0, cached_len, sliding_window, log2_tiles_per_page(block_size),
-                         max_blocks_per_seq * (block_size / 16)};
+                         max_blocks_per_seq * (block_size / 16), pack, q_len};
   return launch_checked_decode(query, kv_cache, block_table, rows, scale, sinks, max_num_kv_splits,
                                workspace, out, q_len, Hq, Hk, num_blocks, max_blocks_per_seq,
                                q_stride_tok, q_stride_head, stream);

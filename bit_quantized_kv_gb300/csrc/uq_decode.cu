@@ -72,7 +72,7 @@ decode_plan(const SeqRows rows, int B, int Hk, int S,
   if (tid < 32) s_hist[tid] = 0;
 
   long long mine = 0;
-  for (int b = tid; b < B; b += kPlanThreads) mine += row_pages(rows, b);
+  for (int b = tid; b < B; b += kPlanThreads) mine += unit_pages(rows, b);
 #pragma unroll
   for (int m = 16; m > 0; m >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, m);
   if (lane == 0) s_part[warp] = mine;
@@ -91,7 +91,7 @@ decode_plan(const SeqRows rows, int B, int Hk, int S,
   if (T < kMinPagesPerUnit) T = kMinPagesPerUnit;
 
   for (int b = tid; b < B; b += kPlanThreads) {
-    const int P = row_pages(rows, b);
+    const int P = unit_pages(rows, b);
     int n = 0, pps = 0, nact = 0;
     if (P > 0) {
       const long long want = (P + T - 1) / T;
@@ -202,6 +202,11 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, c = lane & 3;
+  // O's factor when a row's V reference moves from mu_old to mu_new; a row
+  // that has not seen a token yet (both -inf, GEN only) keeps its zero O.
+  auto rescale_factor = [](float mu_old, float mu_new) {
+    return GEN && mu_old == mu_new ? 1.f : fast_exp2(mu_old - mu_new);
+  };
   const uint32_t smem_base = smem_u32(smem);
   const uint32_t bar_base = smem_base + Lay::kBarOff + warp * NSTAGE * 8;
   const uint32_t stage_base = smem_base + warp * NSTAGE * kTileBytes;
@@ -245,10 +250,28 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
     if (u >= n_units || s_misc[1]) break;
     const uint32_t unit = ws.units[u];
     const int b = (int)(unit & 0xffffu), split = (int)((unit >> 16) & 0xffu), g = (int)(unit >> 24);
-    const int L = row_len(rows, b);
+    const int L = GEN ? unit_len(rows, b) : row_len(rows, b);
     const int pps = ws.seq_info[b].x;
     const int P = (L + kPage - 1) / kPage;
-    const int lo = GEN ? row_lo(rows, L) : 0;   // first token of the window
+    const int lo = GEN ? unit_lo(rows, b) : 0;   // first token of the window
+    // Query rows of the unit: row r is query head g*QG + r % QG of row
+    // b*pack + r / QG (pack > 1 only for multi-query chunk positions).
+    const int pack = GEN ? rows.pack : 1;
+    const int last_row = GEN ? unit_last_row(rows, b) : b;
+    auto row_of = [&](int r) { return GEN ? min(b * pack + r / QG, last_row) : b; };
+    auto row_exists = [&](int r) { return GEN ? r < QG * pack && b * pack + r / QG <= last_row : r < QG; };
+    auto head_of = [&](int r) { return g * QG + (GEN ? r % QG : r); };
+    // this lane's score rows nt*8 + 2c + h: their own token range [rlo, rhi)
+    int rlo[NT][2], rhi[NT][2];
+    if constexpr (GEN) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          rhi[nt][h] = row_len(rows, row_of(nt * 8 + 2 * c + h));
+          rlo[nt][h] = row_lo(rows, rhi[nt][h]);
+        }
+    }
     const int lg_tpp = GEN ? rows.lg_tpp : 0;
     const int p_begin = lo / kPage + split * pps;
     const int p_end = min(p_begin + pps, P);
@@ -299,8 +322,8 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
     for (int r = warp; r < Lay::kRows; r += NWARPS) {
       uint8_t* row = reinterpret_cast<uint8_t*>(qs) + r * Lay::kQRowBytes;
       uint32_t pk[4] = {0u, 0u, 0u, 0u};
-      if (r < QG) {
-        const uint16_t* qp = query + (int64_t)b * q_ss + (int64_t)(g * QG + r) * q_sh + lane * 8;
+      if (row_exists(r)) {
+        const uint16_t* qp = query + (int64_t)row_of(r) * q_ss + (int64_t)head_of(r) * q_sh + lane * 8;
         const uint4 raw = *reinterpret_cast<const uint4*>(qp);
         float x[8];
         const uint32_t uu[4] = {raw.x, raw.y, raw.z, raw.w};
@@ -453,9 +476,20 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
         //    when a page's maximum exceeds the reference by more than
         //    kLazyMaxLog2, so a probability stays below 2^kLazyMaxLog2 (f16 keeps
         //    its full relative precision there) and rescaling O is rare.
-        const int first = lo - page * kPage;   // window start within this page
-        const bool v0 = gq < nvalid && (!GEN || gq >= first);
-        const bool v1 = gq + 8 < nvalid && (!GEN || gq + 8 >= first);
+        // tokens gq and gq + 8 of this page: valid for every score row (plain),
+        // or against each row's own range [rlo, rhi) (GEN)
+        const bool v0 = gq < nvalid, v1 = gq + 8 < nvalid;
+        bool v0r[NT][2], v1r[NT][2];
+        if constexpr (GEN) {
+          const int t0 = page * kPage + gq;
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              v0r[nt][h] = t0 >= rlo[nt][h] && t0 < rhi[nt][h];
+              v1r[nt][h] = t0 + 8 >= rlo[nt][h] && t0 + 8 < rhi[nt][h];
+            }
+        }
         // A lane's own scores decide whether any running maximum can move
         // this page; only then are the row maxima reduced across the 8 lanes
         // of a row.  Otherwise every maximum stays where it is, which is what
@@ -474,8 +508,8 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
           }
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const float s0 = v0 ? sres[h] * fk0 : -INFINITY;
-            const float s1 = v1 ? sres[2 + h] * fk1 : -INFINITY;
+            const float s0 = (GEN ? v0r[nt][h] : v0) ? sres[h] * fk0 : -INFINITY;
+            const float s1 = (GEN ? v1r[nt][h] : v1) ? sres[2 + h] * fk1 : -INFINITY;
             sv[nt][h][0] = s0;
             sv[nt][h][1] = s1;
             uv[nt][h][0] = s0 + evf0;
@@ -501,7 +535,7 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
               const float m_old = m_run[nt][h], mu_old = mu_run[nt][h];
               const float m_new = tmax > m_old + kLazyMaxLog2 ? tmax : m_old;
               const float mu_new = umax > mu_old + kLazyMaxLog2 ? umax : mu_old;
-              l_run[nt][h] *= fast_exp2(m_old - m_new);
+              if (!GEN || m_new != m_old) l_run[nt][h] *= fast_exp2(m_old - m_new);
               mu_prev[nt][h] = mu_old;
               rescale |= mu_new != mu_old;
               m_run[nt][h] = m_new;
@@ -514,9 +548,14 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
           float w4[4];
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            l_run[nt][h] += fast_exp2(sv[nt][h][0] - m_run[nt][h]) + fast_exp2(sv[nt][h][1] - m_run[nt][h]);
-            w4[h] = fast_exp2(uv[nt][h][0] - mu_run[nt][h]);
-            w4[2 + h] = fast_exp2(uv[nt][h][1] - mu_run[nt][h]);
+            // With rows of different lengths in one unit (GEN), a row can meet
+            // a page with none of its tokens before any page with one; its
+            // maxima are still -inf, and 0 stands in so that exp2 gives 0.
+            const float m_ref = GEN && m_run[nt][h] == -INFINITY ? 0.f : m_run[nt][h];
+            const float mu_ref = GEN && mu_run[nt][h] == -INFINITY ? 0.f : mu_run[nt][h];
+            l_run[nt][h] += fast_exp2(sv[nt][h][0] - m_ref) + fast_exp2(sv[nt][h][1] - m_ref);
+            w4[h] = fast_exp2(uv[nt][h][0] - mu_ref);
+            w4[2 + h] = fast_exp2(uv[nt][h][1] - mu_ref);
           }
           pw[nt][0] = movmatrix_trans(pack_f16x2(w4[0], w4[1]));
           pw[nt][1] = movmatrix_trans(pack_f16x2(w4[2], w4[3]));
@@ -530,8 +569,8 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
               tmem_ld32(o_taddr + 32 * q, oc);
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt) {
-                const float a0 = fast_exp2(mu_prev[nt][0] - mu_run[nt][0]);
-                const float a1 = fast_exp2(mu_prev[nt][1] - mu_run[nt][1]);
+                const float a0 = rescale_factor(mu_prev[nt][0], mu_run[nt][0]);
+                const float a1 = rescale_factor(mu_prev[nt][1], mu_run[nt][1]);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                   oc[16 * nt + 4 * e] *= a0;
@@ -545,8 +584,8 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
           } else {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-              const float a0 = fast_exp2(mu_prev[nt][0] - mu_run[nt][0]);
-              const float a1 = fast_exp2(mu_prev[nt][1] - mu_run[nt][1]);
+              const float a0 = rescale_factor(mu_prev[nt][0], mu_run[nt][0]);
+              const float a1 = rescale_factor(mu_prev[nt][1], mu_run[nt][1]);
 #pragma unroll
               for (int mt = 0; mt < 16; ++mt) {
                 o[nt][mt][0] *= a0;
@@ -669,8 +708,14 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
         }
     }
     __syncthreads();
-    if (threadIdx.x < QG) {
+    const int out_rows = QG * pack;   // rows 0 .. out_rows-1 may be written
+    // output row (sequence or chunk position, query head) of unit row r
+    auto out_row = [&](int r) {
+      return GEN ? (int64_t)row_of(r) * Hq + head_of(r) : (int64_t)(b * Hq + g * QG + r);
+    };
+    if (threadIdx.x < out_rows && (!GEN || row_exists(threadIdx.x))) {
       const int r = threadIdx.x;
+      const int64_t orow = out_row(r);
       float M = -INFINITY;
       for (int w = 0; w < NWARPS; ++w) M = fmaxf(M, stats[(w * Lay::kRows + r) * 4]);
       float Ls = 0.f;
@@ -684,7 +729,7 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
         ri[w] = (Ls > 0.f && st[2] > 0.f) ? fast_exp2(st[1] - M) / Ls : 0.f;
       }
       ri[NWARPS] = Ls > 0.f ? M + fast_log2(Ls) : -INFINITY;
-      ws.part_lse[((int64_t)(b * Hq + g * QG + r)) * S + split] = ri[NWARPS];
+      ws.part_lse[orow * S + split] = ri[NWARPS];
     }
     // Lane (gq, c) holds head dims 32gq .. 32gq+31 of rows nt*8 + 2c (+1);
     // the head dims are merged in kMergeParts parts through one buffer.
@@ -725,8 +770,10 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
         }
       }
       __syncthreads();
-      for (int idx = threadIdx.x; idx < QG * (Lay::kPartDims / 4); idx += NWARPS * 32) {
+      for (int idx = threadIdx.x; idx < out_rows * (Lay::kPartDims / 4); idx += NWARPS * 32) {
         const int r = idx / (Lay::kPartDims / 4), d4 = (idx % (Lay::kPartDims / 4)) * 4;
+        if (GEN && !row_exists(r)) continue;
+        const int64_t orow = out_row(r);
         const float* ri = rowinfo + r * (NWARPS + 2);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -738,8 +785,7 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
           acc.z += v.z * f;
           acc.w += v.w * f;
         }
-        *reinterpret_cast<float4*>(ws.part_o + (((int64_t)(b * Hq + g * QG + r)) * S + split) * kHeadDim +
-                                   part * Lay::kPartDims + d4) = acc;
+        *reinterpret_cast<float4*>(ws.part_o + (orow * S + split) * kHeadDim + part * Lay::kPartDims + d4) = acc;
       }
       __syncthreads();  // the merge buffer (the stage buffers) and Q' are free again
     }
@@ -757,13 +803,13 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
 // Stage 2: merge the active splits of each (sequence, query head).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(128)
-decode_stage2(Workspace ws, int B, int Hq, int S, const float* __restrict__ sinks,
+decode_stage2(Workspace ws, int B, int Hq, int S, int pack, const float* __restrict__ sinks,
               uint16_t* __restrict__ out) {
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
   if (row >= B * Hq) return;
   const int b = row / Hq;
-  const int n = ws.seq_info[b].y;
+  const int n = ws.seq_info[b / pack].y;   // row b's unit row holds its split count
   const float* lse = ws.part_lse + (int64_t)row * S;
   float mx = -INFINITY;
   for (int s = lane; s < n; s += 32) mx = fmaxf(mx, lse[s]);
@@ -900,7 +946,7 @@ static cudaError_t launch_plan_and_stage1(const uint16_t* query, int64_t q_ss, i
   CUtensorMap kv_map;
   const int64_t num_slots = (int64_t)num_blocks << (4 + sl.lg_tpp);
   if ((e = make_kv_tensor_map(&kv_map, kv, Hk, num_slots)) != cudaSuccess) return e;
-  decode_plan<<<1, kPlanThreads, 0, stream>>>(sl, B, Hk, S, grid, ws);
+  decode_plan<<<1, kPlanThreads, 0, stream>>>(sl, (B + sl.pack - 1) / sl.pack, Hk, S, grid, ws);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (ev_before && (e = record_timing_event(ev_before, stream)) != cudaSuccess) return e;
   decode_stage1<NT, NWARPS, NSTAGE, GEN><<<grid, NWARPS * 32, Lay::kBytes, stream>>>(
@@ -919,8 +965,8 @@ cudaError_t launch_decode(const uint16_t* query, int64_t q_ss, int64_t q_sh, con
                           void* workspace, uint16_t* out, unsigned* err, cudaStream_t stream,
                           cudaEvent_t ev_before_stage1, cudaEvent_t ev_after_stage1) {
   const Workspace ws = workspace_layout(workspace, B, Hq, S);
-  const bool gen = sl.window > 0 || sl.lg_tpp > 0;
-  const bool wide = Hq / Hk == 16;
+  const bool gen = sl.window > 0 || sl.lg_tpp > 0 || sl.pack > 1;
+  const bool wide = (Hq / Hk) * sl.pack > 8;
   auto run = [&](auto nt, auto g) {
     return launch_plan_and_stage1<decltype(nt)::value, decltype(g)::value>(
         query, q_ss, q_sh, kv, bt, sl, scale, B, Hq, Hk, num_blocks, max_blocks, S, ws, err, stream,
@@ -934,7 +980,7 @@ cudaError_t launch_decode(const uint16_t* query, int64_t q_ss, int64_t q_sh, con
                        : (gen ? run(One{}, Gen{}) : run(One{}, Plain{}));
   if (e != cudaSuccess) return e;
   const int rows = B * Hq;
-  decode_stage2<<<(rows + 3) / 4, 128, 0, stream>>>(ws, B, Hq, S, sinks, out);
+  decode_stage2<<<(rows + 3) / 4, 128, 0, stream>>>(ws, B, Hq, S, sl.pack, sinks, out);
   return cudaGetLastError();
 }
 

@@ -101,6 +101,8 @@ struct SeqRows {
   int window;
   int lg_tpp;
   int cap_tiles;
+  int pack;    // rows (sequences or chunk positions) per work unit: 1, or 2 for multi-query
+  int n_rows;  // rows in the call (B, or the chunk length)
 };
 
 __device__ __forceinline__ int row_len(const SeqRows& r, int b) {
@@ -116,6 +118,19 @@ __device__ __forceinline__ int row_lo(const SeqRows& r, int L) {
 __device__ __forceinline__ int row_pages(const SeqRows& r, int b) {
   const int L = row_len(r, b);
   return (L + kPage - 1) / kPage - row_lo(r, L) / kPage;
+}
+
+// A unit row u covers rows u*pack .. u*pack+pack-1 (those < n_rows).  With
+// pack > 1 the rows are chunk positions, whose lengths grow by one per
+// position, so the unit reads from the first row's window start to the last
+// row's length.
+__device__ __forceinline__ int unit_last_row(const SeqRows& r, int u) {
+  return min(u * r.pack + r.pack - 1, r.n_rows - 1);
+}
+__device__ __forceinline__ int unit_len(const SeqRows& r, int u) { return row_len(r, unit_last_row(r, u)); }
+__device__ __forceinline__ int unit_lo(const SeqRows& r, int u) { return row_lo(r, row_len(r, u * r.pack)); }
+__device__ __forceinline__ int unit_pages(const SeqRows& r, int u) {
+  return (unit_len(r, u) + kPage - 1) / kPage - unit_lo(r, u) / kPage;
 }
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1,

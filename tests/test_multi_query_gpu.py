@@ -59,9 +59,16 @@ def test_matches_oracle_synthetic_batch(cached, q_len, Hq, Hk, S):
     compare(out, ref)
 
 
+def _agree(a: torch.Tensor, b: torch.Tensor):
+    """Two GPU results of the same attention within the decode tolerance
+    (max-abs 1e-2, relative L2 5e-3).  The multi-query entry packs two chunk
+    positions into one 16-row unit (6 or 8 query heads per kv head), so it
+    runs other tiles and splits than uq_decode and is not bit-identical."""
+    compare(a, b.detach().float().cpu().numpy().astype(np.float64).reshape(a.shape))
+
+
 def test_equals_decode_on_the_expanded_batch():
-    """Same kernels, same work list: bit-identical to uq_decode given the
-    materialised synthetic batch."""
+    """Agrees with uq_decode given the materialised synthetic batch."""
     cached, q_len, S = 2047, 6, 16
     wl = workloads.make_decode_workload("mq", 1, 48, 8, np.array([cached + q_len]), 140, S, seed=71)
     cache = fill_cache_gpu(wl)
@@ -72,7 +79,7 @@ def test_equals_decode_on_the_expanded_batch():
     ws = torch.empty(binding.uq_decode_workspace_bytes(q_len, wl.Hq, 256, S), dtype=torch.uint8, device="cuda")
     ref = torch.empty_like(q)
     binding.uq_decode(q, cache, bt, sl, wl.scale, S, ws, ref)
-    assert torch.equal(out, ref)
+    _agree(out, ref)
 
 
 def test_last_row_equals_plain_decode():
@@ -87,7 +94,7 @@ def test_last_row_equals_plain_decode():
     ws = torch.empty(binding.uq_decode_workspace_bytes(1, wl.Hq, 256, S), dtype=torch.uint8, device="cuda")
     ref = torch.empty((1, wl.Hq, 256), dtype=torch.bfloat16, device="cuda")
     binding.uq_decode(q[q_len - 1:].contiguous(), cache, bt, sl, wl.scale, S, ws, ref)
-    assert torch.equal(out[q_len - 1], ref[0])
+    _agree(out[q_len - 1], ref[0])
 
 
 def test_full_size_sampled_rows():
