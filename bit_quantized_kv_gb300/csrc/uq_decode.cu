@@ -69,6 +69,7 @@ decode_plan(const SeqRows rows, int B, int Hk, int S,
   __shared__ long long s_total;
   __shared__ int s_nseq;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_launch_dependents();   // stage 1 may start its set-up now
   if (tid < 32) s_hist[tid] = 0;
 
   long long mine = 0;
@@ -238,6 +239,8 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
     o_taddr = (uint32_t)s_misc[2] + ((uint32_t)(32 * warp) << 16);
   }
 
+  pdl_launch_dependents();   // stage 2 may be scheduled as CTAs retire
+  pdl_wait();                // the plan's work list is complete
   const int n_units = ws.hdr[0];
   uint32_t tiles_done = 0;   // this warp's tiles so far: drives stage and parity
   uint32_t stage_ok = 0;     // bit s: stage s holds a page that was really copied
@@ -807,6 +810,7 @@ decode_stage2(Workspace ws, int B, int Hq, int S, int pack, const float* __restr
               uint16_t* __restrict__ out) {
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
+  pdl_wait();   // stage 1's partials are complete
   if (row >= B * Hq) return;
   const int b = row / Hq;
   const int n = ws.seq_info[b / pack].y;   // row b's unit row holds its split count
@@ -825,13 +829,29 @@ decode_stage2(Workspace ws, int B, int Hq, int S, int pack, const float* __restr
     for (int s0 = 0; s0 < n; s0 += 32) {
       const float wl = (s0 + lane < n) ? fast_exp2(lse[s0 + lane] - mx) : 0.f;
       const int cnt = min(32, n - s0);
-      for (int k = 0; k < cnt; ++k) {
+      auto add = [&](int k, const float4& v0, const float4& v1) {
         const float w = __shfl_sync(0xffffffffu, wl, k);
         den += w;
-        const float4 v0 = *reinterpret_cast<const float4*>(po + (int64_t)(s0 + k) * kHeadDim);
-        const float4 v1 = *reinterpret_cast<const float4*>(po + (int64_t)(s0 + k) * kHeadDim + 4);
         acc[0] += w * v0.x; acc[1] += w * v0.y; acc[2] += w * v0.z; acc[3] += w * v0.w;
         acc[4] += w * v1.x; acc[5] += w * v1.y; acc[6] += w * v1.z; acc[7] += w * v1.w;
+      };
+      // four splits' partials are loaded before any is used, so their
+      // latencies overlap; the sums keep the split order
+      int k = 0;
+      for (; k + 4 <= cnt; k += 4) {
+        float4 v[4][2];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float* pp = po + (int64_t)(s0 + k + i) * kHeadDim;
+          v[i][0] = *reinterpret_cast<const float4*>(pp);
+          v[i][1] = *reinterpret_cast<const float4*>(pp + 4);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) add(k + i, v[i][0], v[i][1]);
+      }
+      for (; k < cnt; ++k) {
+        const float* pp = po + (int64_t)(s0 + k) * kHeadDim;
+        add(k, *reinterpret_cast<const float4*>(pp), *reinterpret_cast<const float4*>(pp + 4));
       }
     }
   }
@@ -858,6 +878,25 @@ static cudaError_t record_timing_event(cudaEvent_t ev, cudaStream_t stream) {
   return cs == cudaStreamCaptureStatusActive
              ? cudaEventRecordWithFlags(ev, stream, cudaEventRecordExternal)
              : cudaEventRecord(ev, stream);
+}
+
+// Launch `kern` so that it may start while the previous kernel on the
+// stream finishes (programmatic stream serialization); the kernel waits in
+// pdl_wait before it reads that kernel's results.
+template <typename... Params, typename... Args>
+static cudaError_t launch_overlapped(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,
+                                     cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 // Per device and instantiation: set the shared-memory opt-in once and size the
@@ -949,10 +988,10 @@ static cudaError_t launch_plan_and_stage1(const uint16_t* query, int64_t q_ss, i
   decode_plan<<<1, kPlanThreads, 0, stream>>>(sl, (B + sl.pack - 1) / sl.pack, Hk, S, grid, ws);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (ev_before && (e = record_timing_event(ev_before, stream)) != cudaSuccess) return e;
-  decode_stage1<NT, NWARPS, NSTAGE, GEN><<<grid, NWARPS * 32, Lay::kBytes, stream>>>(
-      query, q_ss, q_sh, kv_map, bt, sl, scale * kLog2e, Hq, Hk, Hq / Hk, num_blocks, S,
-      ws, err);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  e = launch_overlapped(decode_stage1<NT, NWARPS, NSTAGE, GEN>, dim3(grid), dim3(NWARPS * 32), Lay::kBytes,
+                        stream, query, q_ss, q_sh, kv_map, bt, sl, scale * kLog2e, Hq, Hk, Hq / Hk,
+                        num_blocks, S, ws, err);
+  if (e != cudaSuccess) return e;
   if (ev_after && (e = record_timing_event(ev_after, stream)) != cudaSuccess) return e;
   return cudaSuccess;
 }
@@ -980,8 +1019,8 @@ cudaError_t launch_decode(const uint16_t* query, int64_t q_ss, int64_t q_sh, con
                        : (gen ? run(One{}, Gen{}) : run(One{}, Plain{}));
   if (e != cudaSuccess) return e;
   const int rows = B * Hq;
-  decode_stage2<<<(rows + 3) / 4, 128, 0, stream>>>(ws, B, Hq, S, sl.pack, sinks, out);
-  return cudaGetLastError();
+  return launch_overlapped(decode_stage2, dim3((rows + 3) / 4), dim3(128), 0, stream, ws, B, Hq, S, sl.pack,
+                           sinks, out);
 }
 
 }  // namespace uq

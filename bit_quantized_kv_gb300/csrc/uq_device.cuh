@@ -240,6 +240,17 @@ __device__ __forceinline__ uint4 ldg_nc_128(const void* p) {
   return v;
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the previous kernel on the stream still
+// runs; pdl_wait blocks until that kernel has finished and its writes are
+// visible (a no-op for a kernel launched without the attribute), and
+// pdl_launch_dependents lets the next such kernel start early.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------
 // Tensor memory (TMEM) as per-thread storage.  One warp of the CTA allocates
 // the columns (all 128 lanes) and publishes the base address in shared memory;
