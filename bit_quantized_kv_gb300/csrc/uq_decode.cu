@@ -12,8 +12,9 @@
 // costs a fixed start (first copies in flight, query prologue, merge and
 // partial write) while the last units decide the tail, which grows with
 // the unit size; the sum is smallest near U = sqrt(work per CTA / 2 fixed
-// cost), which with the measured costs is U = sqrt(tiles per CTA / 64),
-// kept in [2, 8].  Sequence b gets n_b = min(S, ceil(P_b / T)) splits
+// cost), which with the measured costs is U = sqrt(tiles per CTA / c),
+// kept in [2, 8], with c = 48 tiles for 6- and 8-row query groups and 64
+// for 16-row ones.  Sequence b gets n_b = min(S, ceil(P_b / T)) splits
 // of whole pages.  Units (sequence, split, kv head) are listed with the
 // longest units first; the plan also resets the unit counter.
 //
@@ -63,7 +64,7 @@ namespace uq {
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kPlanThreads)
 decode_plan(const SeqRows rows, int B, int Hk, int S,
-            int grid, Workspace ws) {
+            int grid, float unit_cost_tiles, Workspace ws) {
   __shared__ long long s_part[kPlanThreads / 32];
   __shared__ int s_hist[32], s_cursor[32], s_wsum[kPlanThreads / 32];
   __shared__ long long s_total;
@@ -86,7 +87,7 @@ decode_plan(const SeqRows rows, int B, int Hk, int S,
   __syncthreads();
   const long long work = s_total * Hk;
   const float per_cta = (float)work / (float)max(grid, 1);
-  const int upc = min(kMaxUnitsPerCta, max(kMinUnitsPerCta, (int)sqrtf(per_cta / kUnitCostTiles)));
+  const int upc = min(kMaxUnitsPerCta, max(kMinUnitsPerCta, (int)sqrtf(per_cta / unit_cost_tiles)));
   const long long target_units = (long long)grid * upc;
   long long T = (work + target_units - 1) / target_units;
   if (T < kMinPagesPerUnit) T = kMinPagesPerUnit;
@@ -985,7 +986,8 @@ static cudaError_t launch_plan_and_stage1(const uint16_t* query, int64_t q_ss, i
   CUtensorMap kv_map;
   const int64_t num_slots = (int64_t)num_blocks << (4 + sl.lg_tpp);
   if ((e = make_kv_tensor_map(&kv_map, kv, Hk, num_slots)) != cudaSuccess) return e;
-  decode_plan<<<1, kPlanThreads, 0, stream>>>(sl, (B + sl.pack - 1) / sl.pack, Hk, S, grid, ws);
+  decode_plan<<<1, kPlanThreads, 0, stream>>>(sl, (B + sl.pack - 1) / sl.pack, Hk, S, grid,
+                                              NT == 2 ? kUnitCostTiles16 : kUnitCostTiles8, ws);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (ev_before && (e = record_timing_event(ev_before, stream)) != cudaSuccess) return e;
   e = launch_overlapped(decode_stage1<NT, NWARPS, NSTAGE, GEN>, dim3(grid), dim3(NWARPS * 32), Lay::kBytes,

@@ -15,8 +15,14 @@ constexpr int kTileBytes = kPage * kSlotBytes;   // 4352 bytes per (tile, kv hea
 #ifndef UQ_MIN_PAGES_PER_UNIT
 #define UQ_MIN_PAGES_PER_UNIT 8
 #endif
-#ifndef UQ_UNIT_COST_TILES
-#define UQ_UNIT_COST_TILES 64
+// Fixed cost of a work unit in tiles, per stage-1 instantiation: the 16-row
+// kernel's unit start and merge cost more (16-row query prologue, tensor
+// memory zeroing, two-part merge).
+#ifndef UQ_UNIT_COST_TILES_8ROW
+#define UQ_UNIT_COST_TILES_8ROW 48
+#endif
+#ifndef UQ_UNIT_COST_TILES_16ROW
+#define UQ_UNIT_COST_TILES_16ROW 64
 #endif
 #ifndef UQ_S1_NSTAGE
 #define UQ_S1_NSTAGE 2
@@ -25,8 +31,12 @@ constexpr int kTileBytes = kPage * kSlotBytes;   // 4352 bytes per (tile, kv hea
 #define UQ_S1_MIN_BLOCKS 4
 #endif
 constexpr int kMinPagesPerUnit = UQ_MIN_PAGES_PER_UNIT;  // floor of 128 tokens per split
-constexpr float kUnitCostTiles = UQ_UNIT_COST_TILES;     // work units per CTA = sqrt(tiles / this)
-constexpr int kMinUnitsPerCta = 2, kMaxUnitsPerCta = 8;
+constexpr float kUnitCostTiles8 = UQ_UNIT_COST_TILES_8ROW;    // work units per CTA = sqrt(tiles / this)
+constexpr float kUnitCostTiles16 = UQ_UNIT_COST_TILES_16ROW;
+#ifndef UQ_MIN_UNITS_PER_CTA
+#define UQ_MIN_UNITS_PER_CTA 2
+#endif
+constexpr int kMinUnitsPerCta = UQ_MIN_UNITS_PER_CTA, kMaxUnitsPerCta = 8;
 constexpr int kStage1Stages = UQ_S1_NSTAGE;              // pages in flight per warp
 // 16-row query groups keep O^T (128 fp32 per lane) in tensor memory: 128
 // columns over all 128 lanes per CTA, each warp in its own 32 lanes.  That
