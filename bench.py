@@ -523,7 +523,7 @@ def run_gpu_mq(args, rank, local, world, dev, stream, peak, peak_kind):
                        "l2": "cache larger than L2 (285 MB per step)"},
             "roofline": {"bound": "hbm", "kernel": "decode_stage1", "achieved": round(ach, 2),
                          "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
-                         "frac": round(ach / peak, 4), "traffic": None,
+                         "frac": round(ach / peak, 4), "traffic": _traffic_from_profile("mq"),
                          "stage1_ms": round(statistics.mean(ms1), 5)},
             "gpu_launches": args.steps * 3, "clocks": clocks.summary(),
             **({} if (rank != 0 or args.no_cpu_baseline) else {"cpu_baseline": _mq_cpu_baseline(args.cpu_budget)})}
