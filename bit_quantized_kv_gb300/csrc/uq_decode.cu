@@ -68,10 +68,14 @@ decode_plan(const SeqRows rows, int B, int Hk, int S,
   __shared__ long long s_part[kPlanThreads / 32];
   __shared__ int s_hist[32], s_cursor[32], s_wsum[kPlanThreads / 32];
   __shared__ long long s_total;
-  __shared__ int s_nseq;
+  __shared__ int s_nseq, s_nact_min, s_nact_max;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   pdl_launch_dependents();   // stage 1 may start its set-up now
   if (tid < 32) s_hist[tid] = 0;
+  if (tid == 0) {
+    s_nact_min = 1 << 30;
+    s_nact_max = 0;
+  }
 
   long long mine = 0;
   for (int b = tid; b < B; b += kPlanThreads) mine += unit_pages(rows, b);
@@ -104,8 +108,25 @@ decode_plan(const SeqRows rows, int B, int Hk, int S,
       atomicAdd(&s_hist[31 - __clz(pps)], 1);
     }
     ws.seq_info[b] = make_int2(pps, nact);
+    atomicMin(&s_nact_min, nact);
+    atomicMax(&s_nact_max, nact);
   }
   __syncthreads();
+  if (rows.mq_base >= 0 && s_nact_min == s_nact_max && s_nact_max > 0) {
+    // Multi-query unit rows read the same pages.  With equal split counts the
+    // units are listed split-major, (split, kv head, unit row), so the units
+    // that read the same pages run side by side and the repeats hit L2.
+    const int per_split = Hk * B, total = s_nact_max * per_split;
+    for (int idx = tid; idx < total; idx += kPlanThreads) {
+      const int s = idx / per_split, rem = idx - s * per_split, g = rem / B, b = rem - g * B;
+      ws.units[idx] = (uint32_t)b | ((uint32_t)s << 16) | ((uint32_t)g << 24);
+    }
+    if (tid == 0) {
+      ws.hdr[0] = total;
+      ws.hdr[1] = 0;
+    }
+    return;
+  }
   if (tid == 0) {
     int acc = 0;
     for (int k = 31; k >= 0; --k) {   // longest splits first
