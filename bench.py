@@ -59,11 +59,38 @@ DEQUANT_SOURCES = ["bit_quantized_kv_gb300/csrc/uq_dequant.cu", "bit_quantized_k
 STORE_SOURCES = ["bit_quantized_kv_gb300/csrc/uq_store.cu", "bit_quantized_kv_gb300/csrc/uq_device.cuh"]
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source with its comments and blank lines removed, so that a
+    comment-only edit does not count as a changed kernel.  String literals
+    are kept as they are (the sources' strings are PTX, which holds no
+    comment markers)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif text[i] == '"':
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(text[i])
+            i += 1
+    lines = [ln.rstrip() for ln in "".join(out).splitlines()]
+    return "\n".join(ln for ln in lines if ln.strip())
+
+
 def _source_hash(sources=None) -> str:
+    """Hash of the code (comments stripped) of the files a profile covers."""
     h = hashlib.sha256()
     for rel in (KERNEL_SOURCES if sources is None else sources):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -16,7 +16,11 @@
 // kept in [2, 8], with c = 48 tiles for 6- and 8-row query groups and 64
 // for 16-row ones.  Sequence b gets n_b = min(S, ceil(P_b / T)) splits
 // of whole pages.  Units (sequence, split, kv head) are listed with the
-// longest units first; the plan also resets the unit counter.
+// longest units first; the plan also resets the unit counter.  For a
+// multi-query chunk the "sequences" are unit rows of one or two chunk
+// positions (SeqRows::pack) that read the same pages; with equal split
+// counts their units are listed split-major so that units reading the same
+// pages run side by side.
 //
 // Stage 1 (persistent: resident CTAs only, 4 warps each).  Each CTA takes
 // units from the counter.  Inside a unit each warp takes every 4th page and
@@ -24,10 +28,11 @@
 // (16 x 272 B, strided by Hk * 272 B in the cache) arrive in shared memory as
 // one TMA tile copy (a 3-D tensor map over the cache: 68 words x Hk heads x
 // slots, box 68 x 1 x 16) completing on a per-stage mbarrier, NSTAGE pages
-// ahead.  One lane issues each copy with warp-uniform operands.  The unit's query group (6, 8 or 16
-// rows) is rotated (fp32 butterfly, x 1/16), rounded through E4M3 and kept
-// in shared memory as f16 in tensor-core operand order.  At the end of the
-// unit the four warps' states are merged into one split partial.
+// ahead.  One lane issues each copy with warp-uniform operands.  The unit's
+// query rows (6, 8 or 16, or two chunk positions of 6 or 8) are rotated
+// (fp32 butterfly, x 1/16), rounded through E4M3 and kept in shared memory
+// as f16 in tensor-core operand order.  At the end of the unit the four
+// warps' states are merged into one split partial.
 //
 // Tensor-core formulation (mma.m16n8k16, f16 in, fp32 accumulate):
 //   QK:  S[t, r] = sum_d K'[t, d] Q'[r, d]      (M = 16 tokens, N = 8 rows)
@@ -43,16 +48,21 @@
 // lane (g = lane/4, c = lane%4) owns head dims [64c, 64c+64) of K (k-step i
 // covers 64c + 4i .. +3) and V head dims [32g, 32g+32) (one UE8M0 block).
 //
-// 16-row query groups (GQA 16) keep O^T in tensor memory instead of
-// registers: 128 fp32 per lane would hold a thread above 168 registers and
-// the SM at 8 warps.  Each CTA allocates 128 TMEM columns over its 128
-// lanes; warp w works in lanes 32w .. 32w+31 only, as per-thread storage.
-// PV loads the 32 columns of one V word (both 8-row tiles), runs its MMAs
-// and stores them back; the rare rescale and the final merge go through the
-// same columns.  At 168 registers three CTAs (12 warps) fit per SM.
+// 16-row query groups keep O^T in tensor memory instead of registers: 128
+// fp32 per lane would hold a thread above 168 registers and the SM at 8
+// warps.  Each CTA allocates 128 TMEM columns over its 128 lanes; warp w
+// works in lanes 32w .. 32w+31 only, as per-thread storage.  PV brings in
+// the O^T columns of one V word in two 16-column halves, each loaded while
+// the previous half's MMAs run, and stores them back; the rare rescale and
+// the final merge go through the same columns.  Three CTAs (12 warps) fit
+// per SM.
 //
 // Stage 2: one warp per (sequence, query head) merges the active splits with
 // the log-sum-exp rule and writes bf16.
+//
+// Stage 1 and stage 2 are launched with programmatic stream serialization:
+// each may start its set-up while the kernel before it finishes, and waits
+// in griddepcontrol.wait before reading that kernel's output.
 #include <type_traits>
 
 #include "uq_decode_common.cuh"
