@@ -39,9 +39,10 @@
 //   PV:  O^T[d, r] += sum_t V'[t, d] W[r, t]    (M = 16 head dims, N = 8 rows)
 // Every FP4 value is c * 2^(e_blk - 127).  For each token t the largest
 // block exponent E_t is factored out, so K' = c * 2^(e_blk - E_t) and
-// V' = c * 2^(e_blk - E_t) are exact in f16 whenever e_blk >= E_t - 23 (a
-// block more than 2^23 below the token's largest block contributes below
-// f16's range and is dropped).  2^(E^K_t - 127) multiplies the scores;
+// V' = c * 2^(e_blk - E_t) are exact in f16 whenever e_blk >= E_t - 14; a
+// block more than 2^14 below the token's largest block is dropped (its
+// share of a score or an output is below 2^-14, and every kept factor is a
+// normal f16).  2^(E^K_t - 127) multiplies the scores;
 // 2^(E^V_t - 127) is added to the exponent of the probability that weights
 // the token's V' row.  The contraction index of QK may be permuted freely as
 // long as Q' and K' agree, which lets every lane read contiguous bytes:
@@ -207,7 +208,7 @@ struct Stage1Layout {
   static constexpr int kRowInfoOff = kStatsOff + kStatsBytes; // [kRows][NWARPS+2] floats
   static constexpr int kRowInfoBytes = kRows * (NWARPS + 2) * 4;
   static constexpr int kLutOff = (kRowInfoOff + kRowInfoBytes + 15) / 16 * 16;
-  static constexpr int kLutBytes = 256 * 4;                  // 2^-delta as f16x2
+  static constexpr int kLutBytes = 0;
   // per warp, per tile: [K, V][token] 8 relative block scales (f16) and one factor
   static constexpr int kMetaRelBytes = 2 * kPage * 16;
   static constexpr int kMetaWarpBytes = kMetaRelBytes + 2 * kPage * 4;
@@ -243,7 +244,6 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
   const uint32_t smem_base = smem_u32(smem);
   const uint32_t bar_base = smem_base + Lay::kBarOff + warp * NSTAGE * 8;
   const uint32_t stage_base = smem_base + warp * NSTAGE * kTileBytes;
-  const uint32_t lut_base = smem_base + Lay::kLutOff;
   const uint32_t meta_rel = smem_base + Lay::kMetaOff + warp * Lay::kMetaWarpBytes;
   const uint32_t meta_f = meta_rel + Lay::kMetaRelBytes;
   volatile int* s_misc = reinterpret_cast<volatile int*>(smem + Lay::kMiscOff);
@@ -253,10 +253,6 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
     for (int i = 0; i < NWARPS * NSTAGE; ++i) mbar_init(smem_base + Lay::kBarOff + 8 * i, 1);
     s_misc[1] = 0;
     fence_barrier_init();
-  }
-  for (int i = threadIdx.x; i < 256; i += NWARPS * 32) {
-    const uint32_t h = pow2_neg_f16(i);
-    reinterpret_cast<uint32_t*>(smem + Lay::kLutOff)[i] = h | (h << 16);
   }
   if constexpr (Lay::kTmemO) {
     if (warp == 0) tmem_alloc(smem_base + Lay::kMiscOff + 8, kTmemCols);
@@ -449,13 +445,16 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
           const int mtok = lane & 15, kind = lane >> 4;
           const uint2 sc = lds64(sb + mtok * kSlotBytes + kKScaleOff + 8 * kind);
           const uint32_t E = max_byte8(sc.x, sc.y);
+          // d = E - byte for all four bytes of a word at once (E is the
+          // largest byte, so no byte borrows), then two per word spread to
+          // halfwords and turned into f16 powers of two
+          const uint32_t E4 = E * 0x01010101u;
+          const uint32_t dx = E4 - sc.x, dy = E4 - sc.y;
           uint32_t p[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t w = k < 2 ? sc.x : sc.y;
-            const uint32_t b0 = (w >> (16 * (k & 1))) & 0xffu, b1 = (w >> (16 * (k & 1) + 8)) & 0xffu;
-            p[k] = (lds32(lut_base + 4 * (E - b0)) & 0xffffu) | (lds32(lut_base + 4 * (E - b1)) & 0xffff0000u);
-          }
+          p[0] = pow2_neg_f16x2(__byte_perm(dx, 0, 0x4140));
+          p[1] = pow2_neg_f16x2(__byte_perm(dx, 0, 0x4342));
+          p[2] = pow2_neg_f16x2(__byte_perm(dy, 0, 0x4140));
+          p[3] = pow2_neg_f16x2(__byte_perm(dy, 0, 0x4342));
           sts128(meta_rel + (kind * kPage + mtok) * 16, make_uint4(p[0], p[1], p[2], p[3]));
           const float f = kind == 0 ? scale_log2e * ue8m0_to_f32(E) : (float)((int)E - 127);
           sts32(meta_f + (kind * kPage + mtok) * 4, __float_as_uint(f));

@@ -118,13 +118,15 @@ __device__ __forceinline__ float ue8m0_to_f32(uint32_t byte) {
   return byte ? __uint_as_float(byte << 23) : __uint_as_float(1u << 22);
 }
 
-// 2^-delta as f16 bits (delta >= 0): exact down to 2^-24, 0 below.
-__device__ __forceinline__ uint32_t pow2_neg_f16(int delta) {
-  delta = delta > 126 ? 126 : delta;
-  float f = __uint_as_float((uint32_t)(127 - delta) << 23);
-  unsigned short h;
-  asm("cvt.rn.f16.f32 %0, %1;" : "=h"(h) : "f"(f));
-  return h;
+// 2^-d as f16 for the two halfwords d0, d1 of d2 (each 0..255), packed as
+// f16x2: the biased exponent 15 - d in bits 14..10 of each half.  d >= 15
+// gives +0: a block more than 2^14 below its token's largest block is
+// dropped, so every kept factor is a normal f16 and the product c * 2^-d of
+// an E2M1 code c stays exact.
+__device__ __forceinline__ uint32_t pow2_neg_f16x2(uint32_t d2) {
+  uint32_t m;
+  asm("min.u16x2 %0, %1, %2;" : "=r"(m) : "r"(d2), "r"(0x000F000Fu));
+  return (m ^ 0x000F000Fu) << 10;   // 15 - m for m in 0..15
 }
 
 // Largest of the eight bytes of (lo, hi).
