@@ -202,3 +202,24 @@ def test_python_binding_rejects_cpu_tensors(lib):
         binding.uq_decode(q, torch.zeros(1, 16, 1, 272, dtype=torch.uint8),
                           torch.zeros(1, 1, dtype=torch.int32), torch.zeros(1, dtype=torch.int32),
                           0.0625, 4, torch.zeros(16, dtype=torch.uint8), q.clone())
+
+
+def test_python_binding_checks_dtypes_and_devices(lib):
+    """The torch-facing wrappers reject wrong dtypes, ranks and host tensors
+    before any call into the library."""
+    import torch
+    cache = torch.zeros(2, 16, 1, 272, dtype=torch.uint8)
+    q = torch.zeros(3, 8, 256, dtype=torch.bfloat16)
+    bt = torch.zeros(2, dtype=torch.int32)
+    ws = torch.zeros(64, dtype=torch.uint8)
+    with pytest.raises(ValueError):           # host tensors
+        binding.uq_decode_multi_query(q, cache, bt, 10, 0.0625, 4, ws, q.clone())
+    with pytest.raises(TypeError):            # fp32 query
+        binding.uq_decode_multi_query(q.float(), cache, bt, 10, 0.0625, 4, ws, q.clone())
+    with pytest.raises(ValueError):           # 2-D block table for one sequence
+        binding.uq_decode_multi_query(q, cache, bt.view(1, 2), 10, 0.0625, 4, ws, q.clone())
+    k = torch.zeros(1, 32, 256, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        binding.uq_full_dequant(cache, bt, k, k.clone())
+    with pytest.raises(TypeError):            # int8 cache (checked first)
+        binding.uq_full_dequant(cache.to(torch.int8), bt, k, k.clone())
