@@ -219,8 +219,11 @@ uq_status uq_decode_ex(const void *query, const void *kv_cache,
  *
  * Row i attends causally to tokens 0 .. cached_len + i: exactly uq_decode
  * on a batch of q_len rows with seq_lens[i] = cached_len + i + 1 that all
- * read the same pages, without materialising those arrays.  Pages shared by
- * the rows are read from HBM once and served to the other rows from L2.
+ * read the same pages, without materialising those arrays.  With 6 or 8
+ * query heads per KV head two consecutive rows share each work unit, so a
+ * page is read and dequantised once per pair of rows; the pairs' units run
+ * side by side, so HBM reads each page about once.  Results equal uq_decode
+ * on that batch within the decode tolerance, not bit for bit.
  * sinks and sliding_window as in uq_decode_ex; the window counts back from
  * each row's own position.  Requires cached_len >= 0 and cached_len + q_len
  * <= max_blocks_per_seq * block_size; q_len == 0 is a no-op.  Other rules as
