@@ -39,6 +39,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "FP4-KV decode attn: achieved HBM GB/s (% of peak), decode tokens/s"
+DEFAULT_WORKLOAD = "outlier_long"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["bit_quantized_kv_gb300/csrc/uq_decode.cu", "bit_quantized_kv_gb300/csrc/uq_decode_common.cuh",
@@ -257,7 +258,7 @@ class DecodeStep:
 
 def run_gpu(args, rank, local, world):
     import torch
-    from bit_quantized_kv_gb300 import binding, workloads
+    from bit_quantized_kv_gb300 import binding
     from bit_quantized_kv_gb300.build import build
 
     torch.cuda.set_device(local)
@@ -275,6 +276,25 @@ def run_gpu(args, rank, local, world):
         return run_gpu_mq(args, rank, local, world, dev, stream, peak, peak_kind)
 
     wl = rank_workload(args.workload, rank, world)
+    line, st = measure_decode(args, wl, dev, stream, peak, peak_kind, local, world)
+    with torch.cuda.stream(stream):
+        # end to end through the public API: pinned host inputs in, output back out
+        line["e2e"] = run_e2e(args, st, stream, torch)
+    del st
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args)
+    if args.workload == DEFAULT_WORKLOAD and not args.headline_only:
+        line["workloads"] = other_workloads(args, rank, local, world, dev, stream, peak, peak_kind)
+    return line
+
+
+def measure_decode(args, wl, dev, stream, peak, peak_kind, local, world):
+    """Time `args.steps` decode steps (store of the B new tokens + decode) of a
+    decode workload after `args.warmup` untimed ones, with stage 1 timed alone
+    on its stream; return (JSON fields, the DecodeStep)."""
+    import torch
+    from bit_quantized_kv_gb300 import binding
     with torch.cuda.stream(stream):
         st = DecodeStep(wl, dev)
         torch.cuda.synchronize()
@@ -291,15 +311,30 @@ def run_gpu(args, rank, local, world):
             run()
         torch.cuda.synchronize()
 
-        # stage-1 events of every timed step (recorded on the launching stream)
         n = args.steps
+        # pass 1: the timed steps, with no event between the kernels (so each
+        # kernel may start while the one before it finishes)
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        _barrier(world)
+        torch.cuda.synchronize()
+        with ClockSampler(local) as clocks:
+            start.record(stream)
+            for _ in range(n):
+                run()
+            end.record(stream)
+            torch.cuda.synchronize()
+        _barrier(world)
+        torch.cuda.synchronize()
+        total_ms = start.elapsed_time(end)
+
+        # pass 2: the same steps with stage 1 bracketed by events on the
+        # launching stream, for the stage-1 roofline
         ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
         ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
         for e in ev_b + ev_a:
             e.record(stream)  # materialise the handles
         torch.cuda.synchronize()
-        start = torch.cuda.Event(enable_timing=True)
-        end = torch.cuda.Event(enable_timing=True)
         if use_graph:
             # re-capture with the timing events inside the graph: one graph per step
             graphs = []
@@ -313,29 +348,20 @@ def run_gpu(args, rank, local, world):
             for g in graphs[:1]:
                 g.replay()
             torch.cuda.synchronize()
-        _barrier(world)
+        for i in range(n):
+            if use_graph:
+                graphs[i].replay()
+            else:
+                binding.uq_set_timing_events(ev_b[i], ev_a[i])
+                st.step()
+        binding.uq_set_timing_events(None, None)
         torch.cuda.synchronize()
-        with ClockSampler(local) as clocks:
-            start.record(stream)
-            for i in range(n):
-                if use_graph:
-                    graphs[i].replay()
-                else:
-                    binding.uq_set_timing_events(ev_b[i], ev_a[i])
-                    st.step()
-            end.record(stream)
-            binding.uq_set_timing_events(None, None)
-            torch.cuda.synchronize()
-        _barrier(world)
-        torch.cuda.synchronize()
-        total_ms = start.elapsed_time(end)
         stage1_ms = [ev_b[i].elapsed_time(ev_a[i]) for i in range(n)]
         flags = binding.uq_check_device_error(stream)
         if flags:
             raise RuntimeError(f"device error flags 0x{flags:x} during the benchmark")
-
-        # end to end through the public API: pinned host inputs in, output back out
-        e2e = run_e2e(args, st, stream, torch)
+        if use_graph:
+            del graphs, graph
 
     total_ms = _max_over_ranks(total_ms, world)
     ms_per_step = total_ms / n
@@ -344,8 +370,6 @@ def run_gpu(args, rank, local, world):
     s1_ms = statistics.mean(stage1_ms)
     kv_bytes = wl.kv_bytes() + wl.B * wl.Hq * wl.D * 2   # stage 1 reads packed KV + query
     achieved = kv_bytes / (s1_ms * 1e-3) / 1e9
-    traffic = _traffic_from_profile(args.workload)
-    clocks_sum = clocks.summary()
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": n, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
@@ -364,15 +388,41 @@ def run_gpu(args, rank, local, world):
                    "parallelism": f"replicas{world}" if world > 1 else "single"},
         "roofline": {"bound": "hbm", "kernel": "decode_stage1", "achieved": round(achieved, 2),
                      "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs",
-                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": _traffic_from_profile(wl.name),
                      "stage1_ms": round(s1_ms, 5), "stage1_bytes": kv_bytes},
-        "e2e": e2e,
         "gpu_launches": n * 4,   # per step: store, plan, stage 1, stage 2
-        "clocks": clocks_sum,
+        "clocks": clocks.summary(),
     }
-    if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl, args)
-    return line
+    return line, st
+
+
+# Workloads timed after the headline in the default run, each in its own
+# section of the JSON line: the other decode configurations, the store, the
+# multi-query continuation chunk and the full-prefix dequantisation.
+EXTRA_WORKLOADS = ("skewed", "batch", "tiny", "store", "mq", "dequant")
+EXTRA_KEYS = ("value", "unit", "ms_per_step", "steps", "warmup", "pct_of_peak", "decode_tokens_per_s",
+              "config", "roofline", "clocks", "gpu_launches")
+
+
+def other_workloads(args, rank, local, world, dev, stream, peak, peak_kind):
+    import torch
+    out = {}
+    for name in EXTRA_WORKLOADS:
+        if name == "store":
+            line = run_gpu_store(args, rank, local, world, dev, stream, peak, peak_kind)
+        elif name == "mq":
+            line = run_gpu_mq(args, rank, local, world, dev, stream, peak, peak_kind, cpu=False)
+        elif name == "dequant":
+            line = run_gpu_dequant(args, rank, local, world, dev, stream, peak, peak_kind, cpu=False)
+        else:
+            line, st = measure_decode(args, rank_workload(name, rank, world), dev, stream, peak,
+                                      peak_kind, local, world)
+            del st
+        out[name] = {k: line[k] for k in EXTRA_KEYS if k in line}
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(args, st, stream, torch):
@@ -449,7 +499,7 @@ def run_gpu_store(args, rank, local, world, dev, stream, peak, peak_kind):
             "gpu_launches": args.steps, "clocks": clocks.summary()}
 
 
-def run_gpu_dequant(args, rank, local, world, dev, stream, peak, peak_kind):
+def run_gpu_dequant(args, rank, local, world, dev, stream, peak, peak_kind, cpu=True):
     """Full-prefix dequantisation of one 32768-token sequence (8 kv heads):
     each step expands its 2048 pages to bf16 K and V (340 MB moved per step,
     above L2)."""
@@ -492,14 +542,14 @@ def run_gpu_dequant(args, rank, local, world, dev, stream, peak, peak_kind):
                          "frac": round(ach / peak, 4),
                          "traffic": _traffic_from_profile("dequant", "full_dequant_dequant.md", DEQUANT_SOURCES)},
             "gpu_launches": args.steps, "clocks": clocks.summary()}
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and cpu and not args.no_cpu_baseline:
         nbytes, secs, desc = _oracle_dequant_sample(wl, args.cpu_budget)
         line["cpu_baseline"] = {"value": round(nbytes / secs / 1e9, 6), "unit": UNIT, "cores": 1,
                                 "kind": "oracle", "sample": desc}
     return line
 
 
-def run_gpu_mq(args, rank, local, world, dev, stream, peak, peak_kind):
+def run_gpu_mq(args, rank, local, world, dev, stream, peak, peak_kind, cpu=True):
     """Multi-query continuation decode: 8 draft tokens after 131072 cached
     tokens of one sequence (GQA 8).  GB/s counts each cached byte once (the
     8 rows share the pages; repeats come from L2)."""
@@ -553,7 +603,7 @@ def run_gpu_mq(args, rank, local, world, dev, stream, peak, peak_kind):
                          "frac": round(ach / peak, 4), "traffic": _traffic_from_profile("mq"),
                          "stage1_ms": round(statistics.mean(ms1), 5)},
             "gpu_launches": args.steps * 3, "clocks": clocks.summary(),
-            **({} if (rank != 0 or args.no_cpu_baseline) else {"cpu_baseline": _mq_cpu_baseline(args.cpu_budget)})}
+            **({} if (rank != 0 or not cpu or args.no_cpu_baseline) else {"cpu_baseline": _mq_cpu_baseline(args.cpu_budget)})}
 
 
 def _oracle_mq_sample(budget_s: float):
@@ -750,13 +800,15 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="outlier_long",
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=["tiny", "batch", "outlier_long", "skewed", "outlier_ncu", "skewed_ncu",
                              "store", "dequant", "mq"])
     ap.add_argument("--impl", default="uq", choices=["uq", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="time only the headline workload (no 'workloads' section)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "uq":
         args.warmup = 3

@@ -108,14 +108,43 @@ def _stream_ptr(stream) -> int | None:
 
 
 def _need(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int) -> None:
+    """dtype and rank of a tensor argument (the device is checked by _on_gpu,
+    after the shape checks, so that those are visible without a GPU)."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if t.dim() != ndim:
         raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def _on_gpu(**tensors) -> None:
+    for name, t in tensors.items():
+        if t is not None and not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def _decode_batch_args(query, kv_cache, block_table, seq_lens, out):
+    """Checks shared by the batch decode wrappers, in the order a caller would
+    fix them: dtypes and ranks, the query/out/cache layout, the block-table
+    and length rows, then the device.  Returns (B, Hq, D, nb, bs, Hk, sb)."""
+    _need(query, "query", torch.bfloat16, 3)
+    _need(kv_cache, "kv_cache", torch.uint8, 4)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(out, "out", torch.bfloat16, 3)
+    B, Hq, D = query.shape
+    if query.stride(2) != 1:
+        raise ValueError("query rows must be contiguous along the head dim")
+    if out.shape != query.shape or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor shaped like query")
+    if not (kv_cache.is_contiguous() and block_table.is_contiguous() and seq_lens.is_contiguous()):
+        raise ValueError("kv_cache, block_table and seq_lens must be contiguous")
+    if block_table.shape[0] < B or seq_lens.shape[0] < B:
+        raise ValueError("block_table / seq_lens have fewer rows than the batch")
+    _on_gpu(query=query, kv_cache=kv_cache, block_table=block_table, seq_lens=seq_lens, out=out)
+    nb, bs, Hk, sb = kv_cache.shape
+    return B, Hq, D, nb, bs, Hk, sb
 
 
 def uq_version() -> int:
@@ -152,6 +181,7 @@ def uq_store(key: torch.Tensor, value: torch.Tensor, kv_cache: torch.Tensor,
     nb, bs, hk2, sb = kv_cache.shape
     if hk2 != Hk:
         raise ValueError("kv_cache head count differs from key")
+    _on_gpu(key=key, value=value, kv_cache=kv_cache, slot_mapping=slot_mapping)
     _check(load().uq_store(key.data_ptr(), value.data_ptr(), kv_cache.data_ptr(),
                            slot_mapping.data_ptr(), N, Hk, D, nb, bs, sb,
                            key.stride(0), value.stride(0), _stream_ptr(stream)))
@@ -167,6 +197,7 @@ def uq_store_rotated_f32(key_rot: torch.Tensor, value: torch.Tensor, kv_cache: t
     if not (key_rot.is_contiguous() and value.is_contiguous() and kv_cache.is_contiguous()
             and slot_mapping.is_contiguous()):
         raise ValueError("uq_store_rotated_f32 needs contiguous tensors")
+    _on_gpu(key_rot=key_rot, value=value, kv_cache=kv_cache, slot_mapping=slot_mapping)
     N, Hk, D = key_rot.shape
     nb, bs, _, sb = kv_cache.shape
     _check(load().uq_store_rotated_f32(key_rot.data_ptr(), value.data_ptr(), kv_cache.data_ptr(),
@@ -181,23 +212,8 @@ def uq_decode(query: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Te
     [num_blocks, 16, Hk, 272]; block_table int32 [B, max_blocks]; seq_lens
     int32 [B]; workspace uint8 (see uq_decode_workspace_bytes); out bf16
     [B, Hq, D] contiguous.  Returns ``out``."""
-    _need(query, "query", torch.bfloat16, 3)
-    _need(kv_cache, "kv_cache", torch.uint8, 4)
-    _need(block_table, "block_table", torch.int32, 2)
-    _need(seq_lens, "seq_lens", torch.int32, 1)
-    _need(out, "out", torch.bfloat16, 3)
-    if not workspace.is_cuda:
-        raise ValueError("workspace must be a CUDA tensor")
-    B, Hq, D = query.shape
-    if query.stride(2) != 1:
-        raise ValueError("query rows must be contiguous along the head dim")
-    if out.shape != query.shape or not out.is_contiguous():
-        raise ValueError("out must be a contiguous tensor shaped like query")
-    if not (kv_cache.is_contiguous() and block_table.is_contiguous() and seq_lens.is_contiguous()):
-        raise ValueError("kv_cache, block_table and seq_lens must be contiguous")
-    nb, bs, Hk, sb = kv_cache.shape
-    if block_table.shape[0] < B or seq_lens.shape[0] < B:
-        raise ValueError("block_table / seq_lens have fewer rows than the batch")
+    B, Hq, D, nb, bs, Hk, sb = _decode_batch_args(query, kv_cache, block_table, seq_lens, out)
+    _on_gpu(workspace=workspace)
     ws_bytes = workspace.numel() * workspace.element_size()
     _check(load().uq_decode(query.data_ptr(), kv_cache.data_ptr(), block_table.data_ptr(),
                             seq_lens.data_ptr(), float(scale), int(max_num_kv_splits),
@@ -213,27 +229,12 @@ def uq_decode_ex(query: torch.Tensor, kv_cache: torch.Tensor, block_table: torch
                  out: torch.Tensor, stream=None) -> torch.Tensor:
     """uq_decode with optional sink logits (fp32 [Hq] CUDA tensor or None)
     and a sliding window (> 0: the last ``sliding_window`` tokens)."""
-    _need(query, "query", torch.bfloat16, 3)
-    _need(kv_cache, "kv_cache", torch.uint8, 4)
-    _need(block_table, "block_table", torch.int32, 2)
-    _need(seq_lens, "seq_lens", torch.int32, 1)
-    _need(out, "out", torch.bfloat16, 3)
-    if not workspace.is_cuda:
-        raise ValueError("workspace must be a CUDA tensor")
-    B, Hq, D = query.shape
+    B, Hq, D, nb, bs, Hk, sb = _decode_batch_args(query, kv_cache, block_table, seq_lens, out)
     if sinks is not None:
         _need(sinks, "sinks", torch.float32, 1)
         if sinks.shape[0] != Hq or not sinks.is_contiguous():
             raise ValueError("sinks must be a contiguous fp32 [Hq] tensor")
-    if query.stride(2) != 1:
-        raise ValueError("query rows must be contiguous along the head dim")
-    if out.shape != query.shape or not out.is_contiguous():
-        raise ValueError("out must be a contiguous tensor shaped like query")
-    if not (kv_cache.is_contiguous() and block_table.is_contiguous() and seq_lens.is_contiguous()):
-        raise ValueError("kv_cache, block_table and seq_lens must be contiguous")
-    nb, bs, Hk, sb = kv_cache.shape
-    if block_table.shape[0] < B or seq_lens.shape[0] < B:
-        raise ValueError("block_table / seq_lens have fewer rows than the batch")
+    _on_gpu(workspace=workspace, sinks=sinks)
     ws_bytes = workspace.numel() * workspace.element_size()
     _check(load().uq_decode_ex(query.data_ptr(), kv_cache.data_ptr(), block_table.data_ptr(),
                                seq_lens.data_ptr(), float(scale),
@@ -257,8 +258,6 @@ def uq_decode_multi_query(query: torch.Tensor, kv_cache: torch.Tensor, block_tab
     _need(kv_cache, "kv_cache", torch.uint8, 4)
     _need(block_table, "block_table", torch.int32, 1)
     _need(out, "out", torch.bfloat16, 3)
-    if not workspace.is_cuda:
-        raise ValueError("workspace must be a CUDA tensor")
     q_len, Hq, D = query.shape
     if query.stride(2) != 1:
         raise ValueError("query rows must be contiguous along the head dim")
@@ -272,6 +271,8 @@ def uq_decode_multi_query(query: torch.Tensor, kv_cache: torch.Tensor, block_tab
         _need(sinks, "sinks", torch.float32, 1)
         if sinks.shape[0] != Hq or not sinks.is_contiguous():
             raise ValueError("sinks must be a contiguous fp32 [Hq] tensor")
+    _on_gpu(query=query, kv_cache=kv_cache, block_table=block_table, out=out, workspace=workspace,
+            sinks=sinks)
     _check(load().uq_decode_multi_query(query.data_ptr(), kv_cache.data_ptr(), block_table.data_ptr(),
                                         int(cached_len), q_len, float(scale),
                                         None if sinks is None else sinks.data_ptr(), int(sliding_window),
@@ -300,6 +301,7 @@ def uq_full_dequant(kv_cache: torch.Tensor, block_table: torch.Tensor, k_out: to
             raise ValueError(f"k_out / v_out must be contiguous [{Hk}, {n * bs}, {HEAD_DIM}]")
     if not (kv_cache.is_contiguous() and block_table.is_contiguous()):
         raise ValueError("kv_cache and block_table must be contiguous")
+    _on_gpu(kv_cache=kv_cache, block_table=block_table, k_out=k_out, v_out=v_out)
     _check(load().uq_full_dequant(kv_cache.data_ptr(), block_table.data_ptr(), n, k_out.data_ptr(),
                                   v_out.data_ptr(), Hk, HEAD_DIM, nb, bs, sb, _stream_ptr(stream)))
     return k_out, v_out
@@ -312,15 +314,7 @@ def uq_decode_static_scratch(query: torch.Tensor, kv_cache: torch.Tensor,
     allocate device memory: the split partials go to the library's fixed
     32 MiB scratch (roughly B * Hq * max_num_kv_splits <= 32480).  Calls that may run
     concurrently on the GPU share that scratch and must not overlap."""
-    _need(query, "query", torch.bfloat16, 3)
-    _need(kv_cache, "kv_cache", torch.uint8, 4)
-    _need(block_table, "block_table", torch.int32, 2)
-    _need(seq_lens, "seq_lens", torch.int32, 1)
-    _need(out, "out", torch.bfloat16, 3)
-    B, Hq, D = query.shape
-    if query.stride(2) != 1 or out.shape != query.shape or not out.is_contiguous():
-        raise ValueError("query rows must be contiguous and out shaped like query")
-    nb, bs, Hk, sb = kv_cache.shape
+    B, Hq, D, nb, bs, Hk, sb = _decode_batch_args(query, kv_cache, block_table, seq_lens, out)
     _check(load().uq_decode_static_scratch(query.data_ptr(), kv_cache.data_ptr(),
                                            block_table.data_ptr(), seq_lens.data_ptr(),
                                            float(scale), int(max_num_kv_splits), out.data_ptr(),

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libuq.so")
 
-SOURCES = ["uq_api.cu", "uq_store.cu", "uq_decode.cu", "uq_dequant.cu", "uq_noalloc.cu"]
+SOURCES = ["uq_api.cu", "uq_store.cu", "uq_decode.cu", "uq_decode_wide.cu", "uq_dequant.cu", "uq_noalloc.cu"]
 HEADERS = ["uq_device.cuh", "uq_decode_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
@@ -39,23 +39,40 @@ def _inputs():
     return paths
 
 
-def _up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def _up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile and link libuq.so if any source changed; return its path."""
-    if not force and _up_to_date():
-        return LIB
+# Test-only variants of the library, built beside it under their own names and
+# never loaded by the package: name -> extra nvcc defines.  "stuck_tile" leaves
+# one page copy of the decode kernel unissued and shortens the bounded waits,
+# so that a test can watch a wait run out and the kernel return.
+VARIANTS = {
+    "stuck_tile": ["-DUQ_TEST_STUCK_TILE", "-DUQ_WAIT_SUSPEND_NS=1024u", "-DUQ_WAIT_SPIN_LIMIT=256u"],
+}
+
+
+def variant_path(name: str) -> str:
+    return os.path.join(BUILD, f"libuq_{name}.so")
+
+
+def build(force: bool = False, verbose: bool = False, variant: str | None = None) -> str:
+    """Compile and link libuq.so (or a test variant of it) if any source
+    changed; return its path."""
+    lib = LIB if variant is None else variant_path(variant)
+    defines = [] if variant is None else VARIANTS[variant]
+    tag = "" if variant is None else f"_{variant}"
+    if not force and _up_to_date(lib):
+        return lib
     os.makedirs(BUILD, exist_ok=True)
     nvcc = _nvcc()
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
-        cmd = [nvcc, *NVCC_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        obj = os.path.join(BUILD, src.replace(".cu", f"{tag}.o"))
+        cmd = [nvcc, *NVCC_FLAGS, *defines, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -67,13 +84,13 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs, "-lpthread", "-ldl", "-lrt"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -8,6 +8,8 @@
 #include <cstring>
 #include <mutex>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include "uq.h"
@@ -24,9 +26,45 @@ cudaError_t launch_decode(const uint16_t* query, int64_t q_ss, int64_t q_sh, con
                           void* workspace, uint16_t* out, unsigned* err, cudaStream_t stream,
                           cudaEvent_t ev_before_stage1, cudaEvent_t ev_after_stage1);
 size_t decode_workspace_bytes(int B, int Hq, int S);
+cudaError_t current_context_id(unsigned long long* id);
 cudaError_t launch_full_dequant(const uint8_t* kv, const int32_t* block_table, int n_pages,
                                 int lg_tpp, int Hk, int num_blocks, uint16_t* k_out, uint16_t* v_out,
                                 unsigned* err, cudaStream_t stream);
+}  // namespace uq
+
+namespace uq {
+// Unique id (cuCtxGetId) of the calling thread's current CUDA context.  A
+// thread with no current context yet gets the current device's primary
+// context (cudaSetDevice initialises and binds it).  Caches keyed by this id
+// are looked up again after a device reset.
+cudaError_t current_context_id(unsigned long long* id) {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  static cudaError_t init_error = cudaSuccess;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    init_error = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q);
+    if (init_error == cudaSuccess && (q != cudaDriverEntryPointSuccess || !fn)) init_error = cudaErrorNotSupported;
+    if (init_error != cudaSuccess) return;
+    get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    fn = nullptr;
+    init_error = cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q);
+    if (init_error == cudaSuccess && (q != cudaDriverEntryPointSuccess || !fn)) init_error = cudaErrorNotSupported;
+    if (init_error == cudaSuccess) get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+  });
+  if (init_error != cudaSuccess) return init_error;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaSetDevice(dev);
+    if (e != cudaSuccess) return e;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return cudaErrorDeviceUninitialized;
+  }
+  return get_id(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorDeviceUninitialized;
+}
 }  // namespace uq
 
 namespace {
@@ -39,9 +77,12 @@ thread_local cudaEvent_t g_ev_before_stage1 = nullptr;
 thread_local cudaEvent_t g_ev_after_stage1 = nullptr;
 
 // The device error word.  Kernels receive its device address; host code
-// obtains that address once per device with cudaGetSymbolAddress.
+// obtains that address with cudaGetSymbolAddress, once per device and CUDA
+// context (a device reset creates a new context, in which the module and its
+// variables live at new addresses).
 __device__ unsigned int g_device_error_word;
 unsigned int* g_err_ptr[kMaxDevices] = {nullptr};
+unsigned long long g_err_ctx[kMaxDevices] = {0};
 std::mutex g_err_mutex;
 
 uq_status fail(uq_status code, const char* fmt, ...) {
@@ -68,18 +109,23 @@ int log2_tiles_per_page(int bs) {
   return lg;
 }
 
-// Device address of the error word on the current device (set-up on first use).
+// Device address of the error word in the current context (looked up on the
+// first use in each context).
 uq_status error_word(unsigned int** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(UQ_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return fail(UQ_ERR_UNSUPPORTED, "device index %d >= %d", dev, kMaxDevices);
+  unsigned long long ctx = 0;
+  if ((e = uq::current_context_id(&ctx)) != cudaSuccess)
+    return fail(UQ_ERR_CUDA, "reading the current context: %s", cudaGetErrorString(e));
   std::lock_guard<std::mutex> lock(g_err_mutex);
-  if (!g_err_ptr[dev]) {
+  if (!g_err_ptr[dev] || g_err_ctx[dev] != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_device_error_word);
     if (e != cudaSuccess) return fail(UQ_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
     g_err_ptr[dev] = static_cast<unsigned int*>(p);
+    g_err_ctx[dev] = ctx;
   }
   *out = g_err_ptr[dev];
   return UQ_OK;
@@ -328,10 +374,10 @@ uq_status uq_decode_multi_query(const void* query, const void* kv_cache, const i
     return fail(UQ_ERR_INVALID_ARG, "cached_len %d + q_len %d exceeds the %d pages of block_table",
                 cached_len, q_len, max_blocks_per_seq);
   if (sinks && !aligned(sinks, 4)) return fail(UQ_ERR_INVALID_ARG, "sinks must be 4-byte aligned");
-  // Two chunk positions share a work unit when their query rows fit one
-  // 16-row group (6 or 8 query heads per kv head): each page is read and
-  // dequantised once for both.
-  const int pack = (q_len > 1 && 2 * (Hq / Hk) <= 16) ? 2 : 1;
+  // Consecutive chunk positions share a work unit, up to 64 query rows
+  // (8 positions of 8 query heads per kv head, 10 of 6, 4 of 16): each page
+  // is read and dequantised once for all of them.
+  const int pack = q_len > 1 ? (64 / (Hq / Hk) < q_len ? 64 / (Hq / Hk) : q_len) : 1;
   const uq::SeqRows rows{nullptr, 0, cached_len, sliding_window, log2_tiles_per_page(block_size),
                          max_blocks_per_seq * (block_size / 16), pack, q_len};
   return launch_checked_decode(query, kv_cache, block_table, rows, scale, sinks, max_num_kv_splits,

@@ -64,7 +64,10 @@
 // Stage 1 and stage 2 are launched with programmatic stream serialization:
 // each may start its set-up while the kernel before it finishes, and waits
 // in griddepcontrol.wait before reading that kernel's output.
+#include <mutex>
 #include <type_traits>
+
+#include <cuda_fp16.h>
 
 #include "uq_decode_common.cuh"
 
@@ -81,6 +84,10 @@ decode_plan(const SeqRows rows, int B, int Hk, int S,
   __shared__ long long s_total;
   __shared__ int s_nseq, s_nact_min, s_nact_max;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // The plan is queued with programmatic serialization, so its launch
+  // overlaps the kernel before it on the stream; everything it reads or
+  // writes waits for that kernel to finish.
+  pdl_wait();
   pdl_launch_dependents();   // stage 1 may start its set-up now
   if (tid < 32) s_hist[tid] = 0;
   if (tid == 0) {
@@ -192,6 +199,67 @@ decode_plan(const SeqRows rows, int B, int Hk, int S,
 // ---------------------------------------------------------------------------
 // Stage 1.
 // ---------------------------------------------------------------------------
+// Exact score contribution of K blocks more than 2^27 below their token's
+// largest block, which the tensor-core pass leaves out (their f16 relative
+// scale would not be exact).  Such spreads never come out of a rotated K in
+// practice; the path exists so that scores stay exact for every cache the
+// store can write.  Lane (gq, c) computes, for tokens gq and gq + 8 of the
+// tile at sb and its score rows nt*8 + 2c + h, the sum over those blocks of
+// 2^(byte - 127) * sum_d E2M1(code_d) * q'[row][d], times scale*log2e, in
+// fp32, and stores it at dst as [nt][h][token] floats.  q' is read back from
+// the operand-order query rows (row stride q_row_bytes: head dim d sits in
+// k-step (d % 64) / 4 at f16 position 2 (d / 64) + (d & 1) + 8 ((d >> 1) & 1)).
+// Out of line and through shared memory, so that the rare path costs the
+// main loop no registers.
+template <int NT>
+__device__ __noinline__ void far_k_blocks(uint32_t sb, uint32_t q_base, int q_row_bytes, int gq, int c,
+                                          float scale_log2e, uint32_t dst) {
+#pragma unroll
+  for (int tt = 0; tt < 2; ++tt) {
+    const uint32_t slot = sb + (gq + 8 * tt) * kSlotBytes;
+    const uint2 sc = lds64(slot + kKScaleOff);
+    const uint32_t E = max_byte8(sc.x, sc.y);
+    float add[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) add[nt][0] = add[nt][1] = 0.f;
+#pragma unroll 1
+    for (int blk = 0; blk < 8; ++blk) {
+      const uint32_t e = ((blk < 4 ? sc.x : sc.y) >> (8 * (blk & 3))) & 0xffu;
+      if (E - e < kRelSpan) continue;
+      float acc[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = 0.f;
+#pragma unroll 1
+      for (int w = 0; w < 4; ++w) {   // 8 head dims per code word
+        uint32_t f[4];
+        f16x2x4_from_e2m1_word(lds32(slot + 16 * blk + 4 * w), f);
+#pragma unroll
+        for (int e8 = 0; e8 < 8; ++e8) {
+          const float kv = __half2float(__ushort_as_half((unsigned short)(f[e8 >> 1] >> (16 * (e8 & 1)))));
+          const int d = 32 * blk + 8 * w + e8;
+          const uint32_t qoff = ((d & 63) >> 2) * 32 + 2 * (2 * (d >> 6) + (d & 1) + 8 * ((d >> 1) & 1));
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t qa = q_base + (nt * 8 + 2 * c + h) * q_row_bytes + qoff;
+              acc[nt][h] = fmaf(kv, __half2float(__ushort_as_half((unsigned short)lds16(qa))), acc[nt][h]);
+            }
+        }
+      }
+      const float bscale = scale_log2e * ue8m0_to_f32(e);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) add[nt][h] = fmaf(acc[nt][h], bscale, add[nt][h]);
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) sts32(dst + 4 * ((nt * 2 + h) * 2 + tt), __float_as_uint(add[nt][h]));
+  }
+}
+
 template <int NT, int NWARPS, int NSTAGE>
 struct Stage1Layout {
   static constexpr int kRows = NT * 8;                       // padded query rows
@@ -207,13 +275,14 @@ struct Stage1Layout {
   static constexpr int kStatsBytes = NWARPS * kRows * 4 * 4;
   static constexpr int kRowInfoOff = kStatsOff + kStatsBytes; // [kRows][NWARPS+2] floats
   static constexpr int kRowInfoBytes = kRows * (NWARPS + 2) * 4;
-  static constexpr int kLutOff = (kRowInfoOff + kRowInfoBytes + 15) / 16 * 16;
-  static constexpr int kLutBytes = 0;
   // per warp, per tile: [K, V][token] 8 relative block scales (f16) and one factor
   static constexpr int kMetaRelBytes = 2 * kPage * 16;
   static constexpr int kMetaWarpBytes = kMetaRelBytes + 2 * kPage * 4;
-  static constexpr int kMetaOff = kLutOff + kLutBytes;
-  static constexpr int kBarOff = kMetaOff + NWARPS * kMetaWarpBytes;
+  static constexpr int kMetaOff = (kRowInfoOff + kRowInfoBytes + 15) / 16 * 16;
+  // per lane: the far-K-block score additions of the rare exact path, [NT][2][2] floats
+  static constexpr int kFixOff = kMetaOff + NWARPS * kMetaWarpBytes;
+  static constexpr int kFixBytes = NWARPS * 32 * NT * 16;
+  static constexpr int kBarOff = kFixOff + kFixBytes;
   static constexpr int kBarBytes = NWARPS * NSTAGE * 8;
   static constexpr int kMiscOff = kBarOff + kBarBytes;       // unit id, abort flag, TMEM base
   static constexpr int kQOff = (kMiscOff + 16 + 127) / 128 * 128;
@@ -236,11 +305,6 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, c = lane & 3;
-  // O's factor when a row's V reference moves from mu_old to mu_new; a row
-  // that has not seen a token yet (both -inf, GEN only) keeps its zero O.
-  auto rescale_factor = [](float mu_old, float mu_new) {
-    return GEN && mu_old == mu_new ? 1.f : fast_exp2(mu_old - mu_new);
-  };
   const uint32_t smem_base = smem_u32(smem);
   const uint32_t bar_base = smem_base + Lay::kBarOff + warp * NSTAGE * 8;
   const uint32_t stage_base = smem_base + warp * NSTAGE * kTileBytes;
@@ -327,13 +391,23 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
       const uint32_t bar = bar_base + 8 * stg;
       const bool ok = (unsigned)pid < (unsigned)num_blocks;
       stage_ok = ok ? (stage_ok | (1u << stg)) : (stage_ok & ~(1u << stg));
+#ifdef UQ_TEST_STUCK_TILE
+      // Test builds only: the first tile of work unit 0's first warp is
+      // announced to its barrier but never copied, so that barrier's phase
+      // cannot complete and the bounded wait on it runs out.  No copy is in
+      // flight for that stage.
+      const bool copy = !(u == 0 && warp == 0 && j == 0);
+#else
+      constexpr bool copy = true;
+#endif
       // the warp has finished reading this stage (callers __syncwarp first)
       if (lane == 0) {
         if (ok) {
           fence_proxy_async_smem();
           mbar_arrive_expect_tx(bar, kTileBytes);
-          tma_load_3d(stage_base + stg * kTileBytes, &kv_map, 0, g,
-                      ((pid << lg_tpp) + (tile & tile_mask)) * kPage, bar);
+          if (copy)
+            tma_load_3d(stage_base + stg * kTileBytes, &kv_map, 0, g,
+                        ((pid << lg_tpp) + (tile & tile_mask)) * kPage, bar);
         } else {
           atomicOr(err, kErrBadPage);
           mbar_arrive(bar);
@@ -411,13 +485,18 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
 #pragma unroll
       for (int q = 0; q < 4; ++q) tmem_st32(o_taddr + 32 * q, z);
     }
-    float m_run[NT][2], mu_run[NT][2], l_run[NT][2];
+    // Per score row: m_run the running score maximum (log2 units), d_run the
+    // V reference relative to it (the probability that weights a token's V'
+    // row is 2^(s - m_run + e_V - d_run)), l_run the sum of 2^(s - m_run).
+    // Keeping the V reference relative to m_run keeps every exponent small
+    // even when the scores themselves are large.
+    float m_run[NT][2], d_run[NT][2], l_run[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         m_run[nt][h] = -INFINITY;
-        mu_run[nt][h] = -INFINITY;
+        d_run[nt][h] = -INFINITY;
         l_run[nt][h] = 0.f;
       }
 
@@ -439,8 +518,12 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
       if (nvalid > 0) {
         const uint32_t sb = stage_base + stg * kTileBytes;
         // -- tile metadata, one (token, K or V) scale row per lane: the token's
-        //    largest block byte E, the 8 relative scales 2^(byte - E) as f16
-        //    and one fp32 factor (K: scale*log2e*2^(E-127); V: E-127)
+        //    largest block byte E, the 8 relative scales 2^(13 + byte - E) as
+        //    f16 and one fp32 factor (K: scale*log2e*2^(E-127-13); V:
+        //    E-127-13).  A K block more than 2^27 below its token's largest
+        //    block gets a relative scale of 0 here and is added back exactly
+        //    by the fix-up below (need_fix, rare).
+        bool need_fix;
         {
           const int mtok = lane & 15, kind = lane >> 4;
           const uint2 sc = lds64(sb + mtok * kSlotBytes + kKScaleOff + 8 * kind);
@@ -451,13 +534,14 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
           const uint32_t E4 = E * 0x01010101u;
           const uint32_t dx = E4 - sc.x, dy = E4 - sc.y;
           uint32_t p[4];
-          p[0] = pow2_neg_f16x2(__byte_perm(dx, 0, 0x4140));
-          p[1] = pow2_neg_f16x2(__byte_perm(dx, 0, 0x4342));
-          p[2] = pow2_neg_f16x2(__byte_perm(dy, 0, 0x4140));
-          p[3] = pow2_neg_f16x2(__byte_perm(dy, 0, 0x4342));
+          p[0] = pow2_rel_f16x2(__byte_perm(dx, 0, 0x4140));
+          p[1] = pow2_rel_f16x2(__byte_perm(dx, 0, 0x4342));
+          p[2] = pow2_rel_f16x2(__byte_perm(dy, 0, 0x4140));
+          p[3] = pow2_rel_f16x2(__byte_perm(dy, 0, 0x4342));
           sts128(meta_rel + (kind * kPage + mtok) * 16, make_uint4(p[0], p[1], p[2], p[3]));
-          const float f = kind == 0 ? scale_log2e * ue8m0_to_f32(E) : (float)((int)E - 127);
+          const float f = kind == 0 ? scale_log2e * ue8m0_rel_to_f32(E) : (float)((int)E - 127 - kRelTop);
           sts32(meta_f + (kind * kPage + mtok) * 4, __float_as_uint(f));
+          need_fix = __any_sync(0xffffffffu, kind == 0 && E - min_byte8(sc.x, sc.y) >= kRelSpan);
         }
         __syncwarp();
         // K relative scales of tokens gq, gq+8 for blocks 2c, 2c+1 as f16x2 (both halves)
@@ -542,38 +626,60 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
           }
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const float s0 = (GEN ? v0r[nt][h] : v0) ? sres[h] * fk0 : -INFINITY;
-            const float s1 = (GEN ? v1r[nt][h] : v1) ? sres[2 + h] * fk1 : -INFINITY;
-            sv[nt][h][0] = s0;
-            sv[nt][h][1] = s1;
-            uv[nt][h][0] = s0 + evf0;
-            uv[nt][h][1] = s1 + evf1;
-            grow |= fmaxf(s0, s1) > m_run[nt][h] + kLazyMaxLog2;
-            grow |= fmaxf(uv[nt][h][0], uv[nt][h][1]) > mu_run[nt][h] + kLazyMaxLog2;
+            sv[nt][h][0] = (GEN ? v0r[nt][h] : v0) ? sres[h] * fk0 : -INFINITY;
+            sv[nt][h][1] = (GEN ? v1r[nt][h] : v1) ? sres[2 + h] * fk1 : -INFINITY;
           }
         }
+        if (need_fix) {   // rare: K blocks beyond the f16 span, added exactly (masked entries stay -inf)
+          const uint32_t fx = smem_base + Lay::kFixOff + (warp * 32 + lane) * (NT * 16);
+          far_k_blocks<NT>(sb, smem_u32(qs), Lay::kQRowBytes, gq, c, scale_log2e, fx);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int tt = 0; tt < 2; ++tt) sv[nt][h][tt] += __uint_as_float(lds32(fx + 4 * ((nt * 2 + h) * 2 + tt)));
+        }
+        // With rows of different lengths in one unit (GEN), a row can meet a
+        // page with none of its tokens before any page with one; its maximum
+        // is still -inf, and 0 stands in so that exp2 gives 0.
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float s0 = sv[nt][h][0], s1 = sv[nt][h][1];
+            const float m_ref = GEN && m_run[nt][h] == -INFINITY ? 0.f : m_run[nt][h];
+            uv[nt][h][0] = (s0 - m_ref) + evf0;
+            uv[nt][h][1] = (s1 - m_ref) + evf1;
+            grow |= fmaxf(s0, s1) > m_run[nt][h] + kLazyMaxLog2;
+            grow |= fmaxf(uv[nt][h][0], uv[nt][h][1]) > d_run[nt][h] + kLazyMaxLog2;
+          }
         bool rescale = false;
-        float mu_prev[NT][2];
+        float alpha[NT][2];   // O's factor where the V reference moved
         if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               float tmax = fmaxf(sv[nt][h][0], sv[nt][h][1]);
+#pragma unroll
+              for (int msk = 4; msk < 32; msk <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, msk));
+              const float m_old = m_run[nt][h], d_old = d_run[nt][h];
+              const float m_new = tmax > m_old + kLazyMaxLog2 ? tmax : m_old;
+              if (!GEN || m_new != m_old) l_run[nt][h] *= fast_exp2(m_old - m_new);
+              const float m_ref = GEN && m_new == -INFINITY ? 0.f : m_new;
+              uv[nt][h][0] = (sv[nt][h][0] - m_ref) + evf0;
+              uv[nt][h][1] = (sv[nt][h][1] - m_ref) + evf1;
               float umax = fmaxf(uv[nt][h][0], uv[nt][h][1]);
 #pragma unroll
-              for (int msk = 4; msk < 32; msk <<= 1) {
-                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, msk));
-                umax = fmaxf(umax, __shfl_xor_sync(0xffffffffu, umax, msk));
-              }
-              const float m_old = m_run[nt][h], mu_old = mu_run[nt][h];
-              const float m_new = tmax > m_old + kLazyMaxLog2 ? tmax : m_old;
-              const float mu_new = umax > mu_old + kLazyMaxLog2 ? umax : mu_old;
-              if (!GEN || m_new != m_old) l_run[nt][h] *= fast_exp2(m_old - m_new);
-              mu_prev[nt][h] = mu_old;
-              rescale |= mu_new != mu_old;
+              for (int msk = 4; msk < 32; msk <<= 1) umax = fmaxf(umax, __shfl_xor_sync(0xffffffffu, umax, msk));
+              // the old V reference, relative to the new maximum
+              const float d_cur = m_old == -INFINITY ? -INFINITY : d_old + (m_old - m_new);
+              const float d_new = umax > d_cur + kLazyMaxLog2 ? umax : d_cur;
+              alpha[nt][h] = d_new == d_cur ? 1.f : fast_exp2(d_cur - d_new);
+              rescale |= d_new != d_cur;
               m_run[nt][h] = m_new;
-              mu_run[nt][h] = mu_new;
+              d_run[nt][h] = d_new;
             }
         }
         uint32_t pw[NT][2];
@@ -582,14 +688,11 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
           float w4[4];
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            // With rows of different lengths in one unit (GEN), a row can meet
-            // a page with none of its tokens before any page with one; its
-            // maxima are still -inf, and 0 stands in so that exp2 gives 0.
             const float m_ref = GEN && m_run[nt][h] == -INFINITY ? 0.f : m_run[nt][h];
-            const float mu_ref = GEN && mu_run[nt][h] == -INFINITY ? 0.f : mu_run[nt][h];
+            const float d_ref = GEN && d_run[nt][h] == -INFINITY ? 0.f : d_run[nt][h];
             l_run[nt][h] += fast_exp2(sv[nt][h][0] - m_ref) + fast_exp2(sv[nt][h][1] - m_ref);
-            w4[h] = fast_exp2(uv[nt][h][0] - mu_ref);
-            w4[2 + h] = fast_exp2(uv[nt][h][1] - mu_ref);
+            w4[h] = fast_exp2(uv[nt][h][0] - d_ref);
+            w4[2 + h] = fast_exp2(uv[nt][h][1] - d_ref);
           }
           pw[nt][0] = movmatrix_trans(pack_f16x2(w4[0], w4[1]));
           pw[nt][1] = movmatrix_trans(pack_f16x2(w4[2], w4[3]));
@@ -603,8 +706,7 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
               tmem_ld32(o_taddr + 32 * q, oc);
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt) {
-                const float a0 = rescale_factor(mu_prev[nt][0], mu_run[nt][0]);
-                const float a1 = rescale_factor(mu_prev[nt][1], mu_run[nt][1]);
+                const float a0 = alpha[nt][0], a1 = alpha[nt][1];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                   oc[16 * nt + 4 * e] *= a0;
@@ -618,8 +720,7 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
           } else {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-              const float a0 = rescale_factor(mu_prev[nt][0], mu_run[nt][0]);
-              const float a1 = rescale_factor(mu_prev[nt][1], mu_run[nt][1]);
+              const float a0 = alpha[nt][0], a1 = alpha[nt][1];
 #pragma unroll
               for (int mt = 0; mt < 16; ++mt) {
                 o[nt][mt][0] *= a0;
@@ -710,7 +811,7 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           m_run[nt][h] = -INFINITY;
-          mu_run[nt][h] = -INFINITY;
+          d_run[nt][h] = -INFINITY;
           l_run[nt][h] = 0.f;
         }
     }
@@ -737,7 +838,7 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
         for (int h = 0; h < 2; ++h) {
           float* st = stats + (warp * Lay::kRows + nt * 8 + 2 * c + h) * 4;
           st[0] = m_run[nt][h];
-          st[1] = mu_run[nt][h];
+          st[1] = d_run[nt][h];
           st[2] = l_run[nt][h];
         }
     }
@@ -760,7 +861,7 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
       float* ri = rowinfo + r * (NWARPS + 2);
       for (int w = 0; w < NWARPS; ++w) {
         const float* st = stats + (w * Lay::kRows + r) * 4;
-        ri[w] = (Ls > 0.f && st[2] > 0.f) ? fast_exp2(st[1] - M) / Ls : 0.f;
+        ri[w] = (Ls > 0.f && st[2] > 0.f) ? fast_exp2((st[0] - M) + st[1]) / Ls : 0.f;
       }
       ri[NWARPS] = Ls > 0.f ? M + fast_log2(Ls) : -INFINITY;
       ws.part_lse[orow * S + split] = ri[NWARPS];
@@ -853,16 +954,24 @@ decode_stage2(Workspace ws, int B, int Hq, int S, int pack, const float* __restr
   // a sink logit joins the denominator only (log2 units like the partials)
   const float zs = sinks ? sinks[row % Hq] * kLog2e : -INFINITY;
   mx = fmaxf(mx, zs);
+  // the denominator first, so that each split enters the sum already
+  // weighted by its share (<= 1): the running sum never exceeds the largest
+  // split output in magnitude, even next to fp32's top
+  float den = 0.f;
+  if (mx > -INFINITY)
+    for (int s = lane; s < n; s += 32) den += fast_exp2(lse[s] - mx);
+#pragma unroll
+  for (int msk = 16; msk > 0; msk >>= 1) den += __shfl_xor_sync(0xffffffffu, den, msk);
+  if (zs > -INFINITY) den += fast_exp2(zs - mx);
+  const float inv = den > 0.f ? 1.f / den : 0.f;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  float den = sinks ? fast_exp2(zs - mx) : 0.f;
   if (n > 0 && mx > -INFINITY) {
     const float* po = ws.part_o + (int64_t)row * S * kHeadDim + lane * 8;
     for (int s0 = 0; s0 < n; s0 += 32) {
-      const float wl = (s0 + lane < n) ? fast_exp2(lse[s0 + lane] - mx) : 0.f;
+      const float wl = (s0 + lane < n) ? fast_exp2(lse[s0 + lane] - mx) * inv : 0.f;
       const int cnt = min(32, n - s0);
       auto add = [&](int k, const float4& v0, const float4& v1) {
         const float w = __shfl_sync(0xffffffffu, wl, k);
-        den += w;
         acc[0] += w * v0.x; acc[1] += w * v0.y; acc[2] += w * v0.z; acc[3] += w * v0.w;
         acc[4] += w * v1.x; acc[5] += w * v1.y; acc[6] += w * v1.z; acc[7] += w * v1.w;
       };
@@ -886,12 +995,11 @@ decode_stage2(Workspace ws, int B, int Hq, int S, int pack, const float* __restr
       }
     }
   }
-  const float inv = (n > 0 && den > 0.f) ? 1.f / den : 0.f;
   uint32_t pk[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(acc[2 * i + 1] * inv), "f"(acc[2 * i] * inv));
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(acc[2 * i + 1]), "f"(acc[2 * i]));
     pk[i] = r;
   }
   *reinterpret_cast<uint4*>(out + (int64_t)row * kHeadDim + lane * 8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -930,17 +1038,25 @@ static cudaError_t launch_overlapped(void (*kern)(Params...), dim3 grid, dim3 bl
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
-// Per device and instantiation: set the shared-memory opt-in once and size the
-// persistent grid from the occupancy the kernel actually gets.
+// Per device, context and instantiation: set the shared-memory opt-in once
+// and size the persistent grid from the occupancy the kernel actually gets.
+// The cache is shared by all host threads, under a lock.
+cudaError_t current_context_id(unsigned long long* id);
+static std::mutex g_grid_mutex;
+
 template <int NT, bool GEN>
 static cudaError_t stage1_grid(int* grid) {
   constexpr int NWARPS = 4, NSTAGE = kStage1Stages;
   using Lay = Stage1Layout<NT, NWARPS, NSTAGE>;
   static int grid_of_device[64] = {0};
+  static unsigned long long ctx_of_device[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64 && grid_of_device[dev] > 0) {
+  unsigned long long ctx = 0;
+  if ((e = current_context_id(&ctx)) != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_grid_mutex);
+  if (dev >= 0 && dev < 64 && grid_of_device[dev] > 0 && ctx_of_device[dev] == ctx) {
     *grid = grid_of_device[dev];
     return cudaSuccess;
   }
@@ -972,24 +1088,28 @@ static cudaError_t stage1_grid(int* grid) {
     if (e != cudaSuccess) return e;
   }
   *grid = sms * (per_sm > 0 ? per_sm : 1);
-  if (dev >= 0 && dev < 64) grid_of_device[dev] = *grid;
+  if (dev >= 0 && dev < 64) {
+    grid_of_device[dev] = *grid;
+    ctx_of_device[dev] = ctx;
+  }
   return cudaSuccess;
 }
 
 // The cache as a 3-D tensor of 32-bit words: x = word within a slot (68),
 // y = kv head (Hk, stride 272 B), z = slot (num_blocks * block_size, stride
 // Hk * 272 B).  One box of 68 x 1 x 16 words is one (16-token tile, kv head).
-static cudaError_t make_kv_tensor_map(CUtensorMap* map, const uint8_t* kv, int Hk, int64_t num_slots) {
+cudaError_t make_kv_tensor_map(CUtensorMap* map, const uint8_t* kv, int Hk, int64_t num_slots) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  if (!encode) {
+  static std::once_flag once;
+  static cudaError_t lookup = cudaSuccess;
+  std::call_once(once, [] {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                     cudaEnableDefault, &q);
-    if (e != cudaSuccess) return e;
-    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
-    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  }
+    lookup = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (lookup == cudaSuccess && (q != cudaDriverEntryPointSuccess || !fn)) lookup = cudaErrorNotSupported;
+    if (lookup == cudaSuccess) encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (lookup != cudaSuccess) return lookup;
   const cuuint64_t dims[3] = {kSlotBytes / 4, (cuuint64_t)Hk, (cuuint64_t)num_slots};
   const cuuint64_t strides[2] = {kSlotBytes, (cuuint64_t)Hk * kSlotBytes};
   const cuuint32_t box[3] = {kSlotBytes / 4, 1, kPage};
@@ -1016,9 +1136,9 @@ static cudaError_t launch_plan_and_stage1(const uint16_t* query, int64_t q_ss, i
   CUtensorMap kv_map;
   const int64_t num_slots = (int64_t)num_blocks << (4 + sl.lg_tpp);
   if ((e = make_kv_tensor_map(&kv_map, kv, Hk, num_slots)) != cudaSuccess) return e;
-  decode_plan<<<1, kPlanThreads, 0, stream>>>(sl, (B + sl.pack - 1) / sl.pack, Hk, S, grid,
-                                              NT == 2 ? kUnitCostTiles16 : kUnitCostTiles8, ws);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  e = launch_overlapped(decode_plan, dim3(1), dim3(kPlanThreads), 0, stream, sl, (B + sl.pack - 1) / sl.pack, Hk,
+                        S, grid, NT == 2 ? kUnitCostTiles16 : kUnitCostTiles8, ws);
+  if (e != cudaSuccess) return e;
   if (ev_before && (e = record_timing_event(ev_before, stream)) != cudaSuccess) return e;
   e = launch_overlapped(decode_stage1<NT, NWARPS, NSTAGE, GEN>, dim3(grid), dim3(NWARPS * 32), Lay::kBytes,
                         stream, query, q_ss, q_sh, kv_map, bt, sl, scale * kLog2e, Hq, Hk, Hq / Hk,
@@ -1029,6 +1149,36 @@ static cudaError_t launch_plan_and_stage1(const uint16_t* query, int64_t q_ss, i
 }
 
 size_t decode_workspace_bytes(int B, int Hq, int S) { return workspace_bytes(B, Hq, S); }
+
+cudaError_t wide_stage1_grid(int rows_per_unit, int* grid);
+cudaError_t launch_wide_stage1(int rows_per_unit, const uint16_t* query, int64_t q_ss, int64_t q_sh,
+                               const CUtensorMap& kv_map, const int32_t* bt, const SeqRows& sl, float scale,
+                               int Hq, int Hk, int num_blocks, int S, const Workspace& ws, unsigned* err,
+                               cudaStream_t stream, int grid);
+
+// Plan, then the warp-specialised stage 1 for units of more than 8 query rows.
+static cudaError_t launch_plan_and_wide_stage1(const uint16_t* query, int64_t q_ss, int64_t q_sh,
+                                               const uint8_t* kv, const int32_t* bt, const SeqRows& sl,
+                                               float scale, int B, int Hq, int Hk, int num_blocks, int S,
+                                               const Workspace& ws, unsigned* err, cudaStream_t stream,
+                                               cudaEvent_t ev_before, cudaEvent_t ev_after) {
+  const int rows_per_unit = (Hq / Hk) * sl.pack;
+  int grid = 0;
+  cudaError_t e = wide_stage1_grid(rows_per_unit, &grid);
+  if (e != cudaSuccess) return e;
+  CUtensorMap kv_map;
+  const int64_t num_slots = (int64_t)num_blocks << (4 + sl.lg_tpp);
+  if ((e = make_kv_tensor_map(&kv_map, kv, Hk, num_slots)) != cudaSuccess) return e;
+  e = launch_overlapped(decode_plan, dim3(1), dim3(kPlanThreads), 0, stream, sl, (B + sl.pack - 1) / sl.pack, Hk,
+                        S, grid, kUnitCostTilesWide, ws);
+  if (e != cudaSuccess) return e;
+  if (ev_before && (e = record_timing_event(ev_before, stream)) != cudaSuccess) return e;
+  e = launch_wide_stage1(rows_per_unit, query, q_ss, q_sh, kv_map, bt, sl, scale, Hq, Hk, num_blocks, S, ws, err,
+                         stream, grid);
+  if (e != cudaSuccess) return e;
+  if (ev_after && (e = record_timing_event(ev_after, stream)) != cudaSuccess) return e;
+  return cudaSuccess;
+}
 
 cudaError_t launch_decode(const uint16_t* query, int64_t q_ss, int64_t q_sh, const uint8_t* kv,
                           const int32_t* bt, const SeqRows& sl, float scale, const float* sinks,
@@ -1044,10 +1194,10 @@ cudaError_t launch_decode(const uint16_t* query, int64_t q_ss, int64_t q_sh, con
         ev_before_stage1, ev_after_stage1);
   };
   using One = std::integral_constant<int, 1>;
-  using Two = std::integral_constant<int, 2>;
   using Gen = std::true_type;
   using Plain = std::false_type;
-  cudaError_t e = wide ? (gen ? run(Two{}, Gen{}) : run(Two{}, Plain{}))
+  cudaError_t e = wide ? launch_plan_and_wide_stage1(query, q_ss, q_sh, kv, bt, sl, scale, B, Hq, Hk, num_blocks,
+                                                     S, ws, err, stream, ev_before_stage1, ev_after_stage1)
                        : (gen ? run(One{}, Gen{}) : run(One{}, Plain{}));
   if (e != cudaSuccess) return e;
   const int rows = B * Hq;

@@ -33,6 +33,11 @@ constexpr int kTileBytes = kPage * kSlotBytes;   // 4352 bytes per (tile, kv hea
 constexpr int kMinPagesPerUnit = UQ_MIN_PAGES_PER_UNIT;  // floor of 128 tokens per split
 constexpr float kUnitCostTiles8 = UQ_UNIT_COST_TILES_8ROW;    // work units per CTA = sqrt(tiles / this)
 constexpr float kUnitCostTiles16 = UQ_UNIT_COST_TILES_16ROW;
+// The warp-specialised kernel for units of 16 to 64 rows runs one CTA per SM.
+#ifndef UQ_UNIT_COST_TILES_WIDE
+#define UQ_UNIT_COST_TILES_WIDE 64
+#endif
+constexpr float kUnitCostTilesWide = UQ_UNIT_COST_TILES_WIDE;
 #ifndef UQ_MIN_UNITS_PER_CTA
 #define UQ_MIN_UNITS_PER_CTA 2
 #endif

@@ -17,6 +17,7 @@
 
 namespace uq {
 uq_status set_error(uq_status code, const char* msg);
+cudaError_t current_context_id(unsigned long long* id);
 }
 
 namespace {
@@ -27,10 +28,12 @@ constexpr size_t kStaticScratchBytes = size_t(32) << 20;
 constexpr int kMaxDevices = 64;
 
 // The scratch itself.  In host code this name is only a host-side stand-in;
-// its device address comes from cudaGetSymbolAddress, once per device.
+// its device address comes from cudaGetSymbolAddress, once per device and
+// CUDA context (after a device reset the array lives at a new address).
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 void* g_scratch_dev_ptr[kMaxDevices] = {nullptr};
+unsigned long long g_scratch_ctx[kMaxDevices] = {0};
 std::mutex g_scratch_mutex;
 
 }  // namespace
@@ -51,17 +54,21 @@ extern "C" uq_status uq_decode_static_scratch(
   if (e != cudaSuccess) return uq::set_error(UQ_ERR_CUDA, "uq_decode_static_scratch: cudaGetDevice failed");
   if (dev < 0 || dev >= kMaxDevices)
     return uq::set_error(UQ_ERR_UNSUPPORTED, "uq_decode_static_scratch: device index out of range");
+  unsigned long long ctx = 0;
+  if (uq::current_context_id(&ctx) != cudaSuccess)
+    return uq::set_error(UQ_ERR_CUDA, "uq_decode_static_scratch: no current CUDA context");
   void* scratch = nullptr;
   {
-    // First call on a device: look up the device address of the array with
-    // that device current.
+    // First call on a device (or in a new context of it): look up the device
+    // address of the array with that device current.
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_dev_ptr[dev]) {
+    if (!g_scratch_dev_ptr[dev] || g_scratch_ctx[dev] != ctx) {
       void* p = nullptr;
       e = cudaGetSymbolAddress(&p, g_static_scratch);
       if (e != cudaSuccess || !p)
         return uq::set_error(UQ_ERR_CUDA, "uq_decode_static_scratch: cudaGetSymbolAddress failed");
       g_scratch_dev_ptr[dev] = p;
+      g_scratch_ctx[dev] = ctx;
     }
     scratch = g_scratch_dev_ptr[dev];
   }

@@ -141,6 +141,7 @@ store_bf16_kernel(const uint16_t* __restrict__ key, const uint16_t* __restrict__
                   uint8_t* __restrict__ kv_cache, const int64_t* __restrict__ slot_mapping,
                   int64_t num_rows, int Hk, int64_t key_stride, int64_t value_stride,
                   int64_t num_slots, unsigned* __restrict__ err) {
+  pdl_launch_dependents();   // a decode plan queued behind the store may be scheduled now
   const int lane = threadIdx.x & 31;
   const int glane = lane & (kLanesPerRow - 1);
   const int64_t row = (int64_t)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 3);
@@ -179,6 +180,7 @@ __global__ void __launch_bounds__(kStoreThreads)
 store_rotated_f32_kernel(const float* __restrict__ key, const float* __restrict__ value,
                          uint8_t* __restrict__ kv_cache, const int64_t* __restrict__ slot_mapping,
                          int64_t num_rows, int Hk, int64_t num_slots, unsigned* __restrict__ err) {
+  pdl_launch_dependents();   // a decode plan queued behind the store may be scheduled now
   const int lane = threadIdx.x & 31;
   const int glane = lane & (kLanesPerRow - 1);
   const int64_t row = (int64_t)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 3);

@@ -223,3 +223,35 @@ def test_python_binding_checks_dtypes_and_devices(lib):
         binding.uq_full_dequant(cache, bt, k, k.clone())
     with pytest.raises(TypeError):            # int8 cache (checked first)
         binding.uq_full_dequant(cache.to(torch.int8), bt, k, k.clone())
+
+
+@pytest.mark.parametrize("wrapper", ["uq_decode", "uq_decode_ex", "uq_decode_static_scratch"])
+def test_batch_decode_wrappers_check_table_layout_before_the_device(lib, wrapper):
+    """Every batch decode wrapper refuses a column slice of the block table
+    (its row stride would be passed as the width) and a block table or
+    seq_lens with fewer rows than the batch (the kernels would read past
+    them), before anything reaches the library or the GPU."""
+    import torch
+    B = 4
+    q = torch.zeros(B, 8, 256, dtype=torch.bfloat16)
+    cache = torch.zeros(8, 16, 1, 272, dtype=torch.uint8)
+    ws = torch.zeros(64, dtype=torch.uint8)
+
+    def call(bt, sl):
+        if wrapper == "uq_decode":
+            binding.uq_decode(q, cache, bt, sl, 0.0625, 4, ws, q.clone())
+        elif wrapper == "uq_decode_ex":
+            binding.uq_decode_ex(q, cache, bt, sl, 0.0625, None, 0, 4, ws, q.clone())
+        else:
+            binding.uq_decode_static_scratch(q, cache, bt, sl, 0.0625, 4, q.clone())
+
+    wide = torch.zeros(B, 6, dtype=torch.int32)
+    lens = torch.zeros(B, dtype=torch.int32)
+    with pytest.raises(ValueError, match="contiguous"):
+        call(wide[:, 1:4], lens)                 # a column slice: row stride 6, width 3
+    with pytest.raises(ValueError, match="fewer rows"):
+        call(wide, lens[:B - 1])                 # seq_lens shorter than the batch
+    with pytest.raises(ValueError, match="fewer rows"):
+        call(wide[:B - 2], lens)                 # block table shorter than the batch
+    with pytest.raises(ValueError, match="CUDA"):
+        call(wide, lens)                         # well formed, but host tensors
