@@ -377,7 +377,8 @@ uq_status uq_decode_multi_query(const void* query, const void* kv_cache, const i
   // Consecutive chunk positions share a work unit, up to 64 query rows
   // (8 positions of 8 query heads per kv head, 10 of 6, 4 of 16): each page
   // is read and dequantised once for all of them.
-  const int pack = q_len > 1 ? (64 / (Hq / Hk) < q_len ? 64 / (Hq / Hk) : q_len) : 1;
+  const int max_rows = uq::kWideKernel ? 64 : 16;
+  const int pack = q_len > 1 ? (max_rows / (Hq / Hk) < q_len ? max_rows / (Hq / Hk) : q_len) : 1;
   const uq::SeqRows rows{nullptr, 0, cached_len, sliding_window, log2_tiles_per_page(block_size),
                          max_blocks_per_seq * (block_size / 16), pack, q_len};
   return launch_checked_decode(query, kv_cache, block_table, rows, scale, sinks, max_num_kv_splits,

@@ -1194,11 +1194,17 @@ cudaError_t launch_decode(const uint16_t* query, int64_t q_ss, int64_t q_sh, con
         ev_before_stage1, ev_after_stage1);
   };
   using One = std::integral_constant<int, 1>;
+  using Two = std::integral_constant<int, 2>;
   using Gen = std::true_type;
   using Plain = std::false_type;
-  cudaError_t e = wide ? launch_plan_and_wide_stage1(query, q_ss, q_sh, kv, bt, sl, scale, B, Hq, Hk, num_blocks,
-                                                     S, ws, err, stream, ev_before_stage1, ev_after_stage1)
-                       : (gen ? run(One{}, Gen{}) : run(One{}, Plain{}));
+  cudaError_t e;
+  if (!wide)
+    e = gen ? run(One{}, Gen{}) : run(One{}, Plain{});
+  else if (kWideKernel)
+    e = launch_plan_and_wide_stage1(query, q_ss, q_sh, kv, bt, sl, scale, B, Hq, Hk, num_blocks, S, ws, err,
+                                    stream, ev_before_stage1, ev_after_stage1);
+  else
+    e = gen ? run(Two{}, Gen{}) : run(Two{}, Plain{});
   if (e != cudaSuccess) return e;
   const int rows = B * Hq;
   return launch_overlapped(decode_stage2, dim3((rows + 3) / 4), dim3(128), 0, stream, ws, B, Hq, S, sl.pack,

@@ -33,6 +33,12 @@ constexpr int kTileBytes = kPage * kSlotBytes;   // 4352 bytes per (tile, kv hea
 constexpr int kMinPagesPerUnit = UQ_MIN_PAGES_PER_UNIT;  // floor of 128 tokens per split
 constexpr float kUnitCostTiles8 = UQ_UNIT_COST_TILES_8ROW;    // work units per CTA = sqrt(tiles / this)
 constexpr float kUnitCostTiles16 = UQ_UNIT_COST_TILES_16ROW;
+// Units of more than 8 rows: the warp-specialised tensor-core kernel (1), or
+// the 16-row mma.sync kernel with at most two query positions per unit (0).
+#ifndef UQ_WIDE_KERNEL
+#define UQ_WIDE_KERNEL 0
+#endif
+constexpr bool kWideKernel = UQ_WIDE_KERNEL != 0;
 // The warp-specialised kernel for units of 16 to 64 rows runs one CTA per SM.
 #ifndef UQ_UNIT_COST_TILES_WIDE
 #define UQ_UNIT_COST_TILES_WIDE 64

@@ -68,6 +68,10 @@ constexpr uint32_t kSoftBar = 1;                      // named barrier of the fo
 constexpr uint32_t kSoftThreads = 128;
 constexpr uint32_t kTmemCols = 512;
 
+// Scores of one chunk of rows (16 or 32 columns) for the thread's token lane.
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[16]) { tmem_ld16(taddr, v); }
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[32]) { tmem_ld32(taddr, v); }
+
 template <int NR>
 struct Layout {
   static_assert(NR == 16 || NR == 32 || NR == 64, "query rows per unit");
@@ -82,8 +86,8 @@ struct Layout {
   static constexpr int kEvfOff = kPbOff + 2 * kPbBytes;   // [2][128] fp32 V exponent e_t
   static constexpr int kGnvOff = kEvfOff + 2 * kGroupTokens * 4;   // [2][8] valid tokens per tile
   static constexpr int kSnvOff = kGnvOff + 2 * kGroupTiles * 4;    // [stage] valid tokens
-  static constexpr int kMetaOff = kSnvOff + kStageTiles * 4;       // [4 warps][16 tokens] f16x2
-  static constexpr int kRowOff = kMetaOff + 4 * kPage * 4;         // rlo[NR], rhi[NR]
+  static constexpr int kMetaOff = kSnvOff + kStageTiles * 4;       // [4 warps][128 tokens] f16x2
+  static constexpr int kRowOff = kMetaOff + 4 * kGroupTokens * 4;  // rlo[NR], rhi[NR]
   static constexpr int kStatOff = kRowOff + 2 * NR * 4;            // m[NR], d[NR]
   static constexpr int kRedOff = kStatOff + 2 * NR * 4;            // [4][2][NR] scratch
   static constexpr int kFacOff = kRedOff + 4 * 2 * NR * 4;         // [NR] factors
@@ -160,6 +164,30 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
   return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, err));
 }
 
+// Non-blocking test of a phase, taken by the whole warp (true only if every
+// lane saw it complete).
+__device__ __forceinline__ bool test_warp(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+  return __all_sync(0xffffffffu, done != 0);
+}
+
+// One short suspended wait for a phase (returns when it completes or after
+// about kPollNs); the caller re-tests what it is waiting for.  kPollLimit
+// such polls take about as long as one full bounded wait.
+constexpr uint32_t kPollNs = 256;
+constexpr uint32_t kPollLimit = kWaitSpinLimit * (kWaitSuspendNs > kPollNs ? kWaitSuspendNs / kPollNs : 1u);
+__device__ __forceinline__ void poll_bar(uint32_t bar, uint32_t parity) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%0], %1, %2;\n}\n"
+      :: "r"(bar), "r"(parity), "r"(kPollNs) : "memory");
+}
+
 // Head dim held by tensor-memory lane `l` (0..31) of quarter q in half h of
 // the PV operands: the convert warps place dims 64q + 8g + 4h + 2mt + r at
 // lane 16mt + 8r + g (g = 0..7, mt, r = 0..1).
@@ -174,6 +202,7 @@ decode_stage1_wide(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_s
                    const SeqRows rows, float scale_log2e, int Hq, int Hk, int num_blocks, int S,
                    Workspace ws, unsigned* __restrict__ err) {
   using Lay = Layout<NR>;
+  constexpr int kChunk = NR < 32 ? NR : 32;   // softmax rows per tensor-memory load
   constexpr int KST = Lay::kStageTiles;
   constexpr int NS = Lay::kNS;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -223,6 +252,7 @@ decode_stage1_wide(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_s
   int published = 0, pending = -1;   // producer: units handed to the ring; one taken but not handed
   if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- producer
+    if (lane == 0) asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&kv_map)) : "memory");
     uint32_t tc = 0;
     const int lg = rows.lg_tpp, tmask = (1 << lg) - 1;
     for (;;) {
@@ -246,44 +276,48 @@ decode_stage1_wide(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_s
       ++published;
       const Unit U = decode_unit(rows, ws, u);
       const int32_t* bt_row = block_table + (int64_t)U.b * rows.bt_stride;
+      // A group of up to 8 tiles at a time: lane i waits for its tile's stage
+      // buffer and issues that tile's copy, so the copies of a group leave
+      // together; the page ids of the next group are loaded a group ahead.
       bool aborted = false;
-      for (int j0 = 0; j0 < U.n_tiles && !aborted; j0 += 32) {
-        const int jj = j0 + lane;
-        const int pid_l = jj < U.n_tiles ? bt_row[(U.p_begin + jj) >> lg] : -1;
-        const int jn = min(32, U.n_tiles - j0);
-        for (int k = 0; k < jn; ++k) {
-          const int pid = __shfl_sync(0xffffffffu, pid_l, k);
-          const int tile = U.p_begin + j0 + k;
-          const uint32_t slot = tc % KST;
-          if (!wait_warp(bar(Lay::bEmpty + slot), ((tc / KST) & 1u) ^ 1u, abort_flag, err)) {
-            aborted = true;
-            break;
-          }
-#ifdef UQ_TEST_STUCK_TILE
-          // Test builds only: the first tile of work unit 0 is announced to
-          // its barrier but never copied, so that barrier's phase cannot
-          // complete and the bounded waits on it run out.  No copy is in
-          // flight for that stage.
-          const bool copy = !(u == 0 && j0 + k == 0);
-#else
-          constexpr bool copy = true;
-#endif
-          if (lane == 0) {
-            const bool ok = (unsigned)pid < (unsigned)num_blocks;
-            reinterpret_cast<volatile int*>(smem + Lay::kSnvOff)[slot] = ok ? min(kPage, U.L - tile * kPage) : 0;
-            if (ok) {
-              fence_proxy_async_smem();
-              mbar_arrive_expect_tx(bar(Lay::bFull + slot), kTileBytes);
-              if (copy)
-                tma_load_3d(stage(slot), &kv_map, 0, U.g, ((pid << lg) + (tile & tmask)) * kPage,
-                            bar(Lay::bFull + slot));
-            } else {
-              atomicOr(err, kErrBadPage);
-              mbar_arrive(bar(Lay::bFull + slot));
-            }
-          }
-          ++tc;
+      int pid_next = lane < min(kGroupTiles, U.n_tiles) ? bt_row[(U.p_begin + lane) >> lg] : -1;
+      for (int j0 = 0; j0 < U.n_tiles; j0 += kGroupTiles) {
+        const int n_here = min(kGroupTiles, U.n_tiles - j0);
+        const int pid = pid_next;
+        const int jn = j0 + kGroupTiles + lane;
+        pid_next = (lane < kGroupTiles && jn < U.n_tiles) ? bt_row[(U.p_begin + jn) >> lg] : -1;
+        const uint32_t t_i = tc + (uint32_t)lane, slot = t_i % KST;
+        bool got = true;
+        if (lane < n_here) got = wait_bar(bar(Lay::bEmpty + slot), ((t_i / KST) & 1u) ^ 1u, abort_flag, err);
+        if (!__all_sync(0xffffffffu, got)) {
+          aborted = true;
+          break;
         }
+#ifdef UQ_TEST_STUCK_TILE
+        // Test builds only: the first tile of work unit 0 is announced to its
+        // barrier but never copied, so that barrier's phase cannot complete
+        // and the bounded waits on it run out.  No copy is in flight for that
+        // stage.
+        const bool copy = !(u == 0 && j0 + lane == 0);
+#else
+        constexpr bool copy = true;
+#endif
+        if (lane < n_here) {
+          const int tile = U.p_begin + j0 + lane;
+          const bool ok = (unsigned)pid < (unsigned)num_blocks;
+          reinterpret_cast<volatile int*>(smem + Lay::kSnvOff)[slot] = ok ? min(kPage, U.L - tile * kPage) : 0;
+          if (ok) {
+            // the stage's previous contents were only read (generic proxy),
+            // and the empty barrier orders those reads before this copy
+            mbar_arrive_expect_tx(bar(Lay::bFull + slot), kTileBytes);
+            if (copy)
+              tma_load_3d(stage(slot), &kv_map, 0, U.g, ((pid << lg) + (tile & tmask)) * kPage, bar(Lay::bFull + slot));
+          } else {
+            atomicOr(err, kErrBadPage);
+            mbar_arrive(bar(Lay::bFull + slot));
+          }
+        }
+        tc += (uint32_t)n_here;
       }
       if (aborted) break;
     }
@@ -295,87 +329,133 @@ decode_stage1_wide(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_s
     }
   } else if (warp == kMmaWarp) {
     // --------------------------------------------------------------- tensor core
-    if (lane == 0) {
-      // QK: A = K codes E2M1 (format 5), B = q' E4M3 (format 0), UE8M0 scales,
-      // N = NR, M = 128; the scale byte of each operand is picked per block.
-      const uint32_t idesc_qk = (5u << 7) | ((uint32_t)(NR >> 3) << 17) | (1u << 23) |
-                                ((uint32_t)(kGroupTokens >> 4) << 24);
-      // PV: D fp32, A and B f16, B (P^T) stored rows-contiguous (MN-major),
-      // N = NR, M = 128 head dims.
-      const uint32_t idesc_pv = (1u << 4) | (1u << 16) | ((uint32_t)(NR >> 3) << 17) | (8u << 24);
-      int un = 0;
-      uint32_t gc = 0;
-      uint32_t last_bar = 0, last_parity = 0;
-      bool issued = false;
-      for (;;) {
-        const int us = un & 3;
-        if (!wait_bar(bar(Lay::bUFull + us), (un >> 2) & 1, abort_flag, err)) break;
-        const int u = s_unit[us];
-        if (u < 0) break;
-        const Unit U = decode_unit(rows, ws, u);
-        if (!wait_bar(bar(Lay::bQFull), un & 1, abort_flag, err)) break;
-        bool aborted = false;
-        for (int grp = 0; grp <= U.n_groups; ++grp) {
-          if (grp < U.n_groups) {
-            const uint32_t cg = gc + grp, buf = cg & 1u, sb = cg % NS;
-            if (!wait_bar(bar(Lay::bConv + buf), (cg >> 1) & 1u, abort_flag, err) ||
-                !wait_bar(bar(Lay::bSFree + sb), ((cg / NS) & 1u) ^ 1u, abort_flag, err)) {
-              aborted = true;
-              break;
-            }
+    // The whole warp walks the schedule and takes every wait; lane 0 issues
+    // the tensor-core instructions and their commits.
+    // QK: A = K codes E2M1 (format 5), B = q' E4M3 (format 0), UE8M0 scales,
+    // N = NR, M = 128; the scale byte of each operand is picked per block.
+    const uint32_t idesc_qk = (5u << 7) | ((uint32_t)(NR >> 3) << 17) | (1u << 23) |
+                              ((uint32_t)(kGroupTokens >> 4) << 24);
+    // PV: D fp32, A and B f16, B (P^T) stored rows-contiguous (MN-major),
+    // N = NR, M = 128 head dims.
+    const uint32_t idesc_pv = (1u << 4) | (1u << 16) | ((uint32_t)(NR >> 3) << 17) | (8u << 24);
+    int un = 0;
+    uint32_t gc = 0;
+    uint32_t last_bar = 0, last_parity = 0;
+    bool issued = false;
+    for (;;) {
+      const int us = un & 3;
+      if (!wait_warp(bar(Lay::bUFull + us), (un >> 2) & 1, abort_flag, err)) break;
+      const int u = s_unit[us];
+      if (u < 0) break;
+      const Unit U = decode_unit(rows, ws, u);
+      if (!wait_warp(bar(Lay::bQFull), un & 1, abort_flag, err)) break;
+      // Event driven: QK of the next group goes out as soon as its operands
+      // are converted and its score buffer is free, PV of the oldest scored
+      // group as soon as its P tile is written, whichever comes first.
+      bool aborted = false;
+      int qk = 0, pv = 0;
+      uint32_t idle = 0;
+      while (pv < U.n_groups) {
+        bool moved = false;
+        if (qk < U.n_groups) {
+          const uint32_t cg = gc + qk, buf = cg & 1u, sb = cg % NS;
+          if (test_warp(bar(Lay::bConv + buf), (cg >> 1) & 1u) &&
+              test_warp(bar(Lay::bSFree + sb), ((cg / NS) & 1u) ^ 1u)) {
             tc_fence_after_sync();
-            const uint32_t ka = sbase + Lay::kKaOff + buf * kKaBytes, qb = sbase + Lay::kQbOff;
+            if (lane == 0) {
+              const uint32_t ka = sbase + Lay::kKaOff + buf * kKaBytes, qb = sbase + Lay::kQbOff;
 #pragma unroll
-            for (int kb = 0; kb < 8; ++kb) {
-              const uint64_t ad = smem_desc(ka + kb * 2 * kKaChunk, kKaChunk, 128);
-              const uint64_t bd = smem_desc(qb + kb * 2 * Lay::kQbChunk, Lay::kQbChunk, 128);
-              const uint32_t id = idesc_qk | ((uint32_t)(kb & 3) << 29) | ((uint32_t)(kb & 3) << 4);
-              tc_mma_block_scaled(tmem + Lay::kTmS + sb * NR, ad, bd, id,
-                                  tmem + Lay::kTmSfa + 8 * buf + 4 * (kb >> 2), tmem + Lay::kTmSfb + 4 * (kb >> 2),
-                                  kb > 0 ? 1u : 0u);
+              for (int kb = 0; kb < 8; ++kb) {
+                const uint64_t ad = smem_desc(ka + kb * 2 * kKaChunk, kKaChunk, 128);
+                const uint64_t bd = smem_desc(qb + kb * 2 * Lay::kQbChunk, Lay::kQbChunk, 128);
+                const uint32_t id = idesc_qk | ((uint32_t)(kb & 3) << 29) | ((uint32_t)(kb & 3) << 4);
+                tc_mma_block_scaled(tmem + Lay::kTmS + sb * NR, ad, bd, id,
+                                    tmem + Lay::kTmSfa + 8 * buf + 4 * (kb >> 2), tmem + Lay::kTmSfb + 4 * (kb >> 2),
+                                    kb > 0 ? 1u : 0u);
+              }
+              tc_commit(bar(Lay::bSFull + sb));
+              tc_commit(bar(Lay::bKaFree + buf));
             }
-            tc_commit(bar(Lay::bSFull + sb));
-            tc_commit(bar(Lay::bKaFree + buf));
+            __syncwarp();
             last_bar = bar(Lay::bKaFree + buf);
             last_parity = (cg >> 1) & 1u;
             issued = true;
-          }
-          if (grp > 0) {
-            const uint32_t pg = gc + grp - 1, buf = pg & 1u;
-            if (!wait_bar(bar(Lay::bPFull + buf), (pg >> 1) & 1u, abort_flag, err)) {
-              aborted = true;
-              break;
-            }
-            tc_fence_after_sync();
-            const uint32_t pb = sbase + Lay::kPbOff + buf * Lay::kPbBytes;
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-              for (int ks = 0; ks < 8; ++ks)
-                tc_mma_f16_tmem_a(tmem + Lay::kTmO + h * NR, tmem + Lay::kTmVt + 64 * (2 * buf + h) + 8 * ks,
-                                  smem_desc(pb + ks * 256, 128, kPbNGroup), idesc_pv,
-                                  (grp > 1 || ks > 0) ? 1u : 0u);
-            tc_commit(bar(Lay::bPvDone + buf));
-            last_bar = bar(Lay::bPvDone + buf);
-            last_parity = (pg >> 1) & 1u;
+            ++qk;
+            moved = true;
           }
         }
-        if (aborted) break;
-        gc += (uint32_t)U.n_groups;
-        mbar_arrive(bar(Lay::bUEmpty + us));
-        ++un;
+        if (pv < qk) {
+          const uint32_t pg = gc + pv, buf = pg & 1u;
+          if (test_warp(bar(Lay::bPFull + buf), (pg >> 1) & 1u)) {
+            tc_fence_after_sync();
+            if (lane == 0) {
+              const uint32_t pb = sbase + Lay::kPbOff + buf * Lay::kPbBytes;
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                  tc_mma_f16_tmem_a(tmem + Lay::kTmO + h * NR, tmem + Lay::kTmVt + 64 * (2 * buf + h) + 8 * ks,
+                                    smem_desc(pb + ks * 256, 128, kPbNGroup), idesc_pv,
+                                    (pv > 0 || ks > 0) ? 1u : 0u);
+              tc_commit(bar(Lay::bPvDone + buf));
+            }
+            __syncwarp();
+            last_bar = bar(Lay::bPvDone + buf);
+            last_parity = (pg >> 1) & 1u;
+            ++pv;
+            moved = true;
+          }
+        }
+        if (moved) {
+          idle = 0;
+          continue;
+        }
+        // nothing ready: sleep on the oldest outstanding event (woken early
+        // when it completes), bounded like every other wait
+        if (*abort_flag || ++idle > kPollLimit) {
+          if (idle > kPollLimit) {
+            *abort_flag = 1;
+            atomicOr(err, kErrTimeout);
+          }
+          aborted = true;
+          break;
+        }
+        if (pv < qk) {
+          const uint32_t pg = gc + pv;
+          poll_bar(bar(Lay::bPFull + (pg & 1u)), (pg >> 1) & 1u);
+        } else {
+          const uint32_t cg = gc + qk;
+          poll_bar(bar(Lay::bConv + (cg & 1u)), (cg >> 1) & 1u);
+        }
       }
-      // all tensor-core work this thread issued has completed before the CTA ends
-      if (issued) (void)mbar_wait(last_bar, last_parity);
+      if (aborted) break;
+      gc += (uint32_t)U.n_groups;
+      if (lane == 0) mbar_arrive(bar(Lay::bUEmpty + us));
+      ++un;
     }
+    // all tensor-core work this warp issued has completed before the CTA ends
+    if (issued) (void)mbar_wait(last_bar, last_parity);
   } else if (warp < kSoftWarp0) {
     // ------------------------------------------------------------------ convert
+    // A group at a time: wait for its tiles, then the scale metadata of all
+    // 128 tokens (four tokens per lane), then the eight tiles as straight-line
+    // code whose loads and conversions the scheduler can overlap, then the
+    // release of the tiles' stage buffers.
     const int cq = warp & 3;                 // lane quarter: K tiles 2cq, 2cq+1; V dims 64cq ..
+    // Shared memory through ordinary loads and stores (addresses in the
+    // shared window), which the compiler may batch and reorder; the mbarrier
+    // waits and __syncwarp order them where it matters.
+    auto ld32 = [&](uint32_t a) { return *reinterpret_cast<const uint32_t*>(smem + (a - sbase)); };
+    auto ld64 = [&](uint32_t a) { return *reinterpret_cast<const uint2*>(smem + (a - sbase)); };
+    auto ld128 = [&](uint32_t a) { return *reinterpret_cast<const uint4*>(smem + (a - sbase)); };
+    auto st32 = [&](uint32_t a, uint32_t v) { *reinterpret_cast<uint32_t*>(smem + (a - sbase)) = v; };
+    auto st128 = [&](uint32_t a, uint4 v) { *reinterpret_cast<uint4*>(smem + (a - sbase)) = v; };
     const int gq = lane >> 2, c = lane & 3;
-    const uint32_t meta = sbase + Lay::kMetaOff + cq * 64;
+    const uint32_t meta = sbase + Lay::kMetaOff + cq * (kGroupTokens * 4);
     const uint32_t lane_q = (uint32_t)(32 * cq) << 16;
     const uint32_t voff = kVCodeOff + 32 * cq + 4 * gq;
     const uint32_t half_sel = gq < 4 ? 0x5410u : 0x7632u;   // factor of block 2cq or 2cq+1
+    const uint32_t vsh = 16u * (cq & 1);                     // blocks 2cq, 2cq+1 in their scale word
     int un = 0;
     uint32_t tc = 0, gc = 0;
     bool aborted = false;
@@ -387,57 +467,71 @@ decode_stage1_wide(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_s
       const Unit U = decode_unit(rows, ws, u);
       for (int grp = 0; grp < U.n_groups; ++grp) {
         const uint32_t buf = gc & 1u, ph = (gc >> 1) & 1u;
+        const int n_here = min(kGroupTiles, U.n_tiles - grp * kGroupTiles);
         if (!wait_warp(bar(Lay::bKaFree + buf), ph ^ 1u, abort_flag, err) ||
             !wait_warp(bar(Lay::bPvDone + buf), ph ^ 1u, abort_flag, err)) {
           aborted = true;
           break;
         }
-        tc_fence_after_sync();
-        uint32_t sfw0 = 0, sfw1 = 0;   // K scale bytes of this lane's token (lane quarter cq)
+        int nv[kGroupTiles];
+        uint32_t sb[kGroupTiles];
+#pragma unroll
         for (int i = 0; i < kGroupTiles; ++i) {
-          const int j = grp * kGroupTiles + i;
-          const bool mine = (i >> 1) == cq;
-          const uint32_t vt = tmem + lane_q + Lay::kTmVt + 64 * (2 * buf) + 8 * i;
-          uint32_t slot = 0;
-          int nv = 0;
-          if (j < U.n_tiles) {
-            slot = tc % KST;
-            if (!wait_warp(bar(Lay::bFull + slot), (tc / KST) & 1u, abort_flag, err)) {
-              aborted = true;
-              break;
-            }
-            nv = reinterpret_cast<volatile int*>(smem + Lay::kSnvOff)[slot];
+          const uint32_t t_i = tc + (uint32_t)i, slot = t_i % KST;
+          sb[i] = stage(slot);
+          nv[i] = 0;
+          if (i < n_here) {
+            if (!wait_warp(bar(Lay::bFull + slot), (t_i / KST) & 1u, abort_flag, err)) aborted = true;
+            nv[i] = reinterpret_cast<volatile int*>(smem + Lay::kSnvOff)[slot];
           }
-          if (nv > 0) {
-            const uint32_t sb = stage(slot);
-            if (lane < 16) {
-              // token `lane`: its largest V block byte and the relative scales
-              // of blocks 2cq and 2cq+1
-              const uint2 sc = lds64(sb + lane * kSlotBytes + kVScaleOff);
-              const uint32_t E = max_byte8(sc.x, sc.y);
-              const uint32_t w = cq < 2 ? sc.x : sc.y;
-              const uint32_t sh = 16u * (cq & 1);
-              const uint32_t b0 = (w >> sh) & 0xffu, b1 = (w >> (sh + 8)) & 0xffu;
-              sts32(meta + 4 * lane, pow2_rel_f16x2((E - b0) | ((E - b1) << 16)));
-              if (mine)
-                sts32(sbase + Lay::kEvfOff + (buf * kGroupTokens + 16 * i + lane) * 4,
-                      __float_as_uint((float)((int)E - 127 - kRelTop)));
-            }
-            if (mine && (lane >> 4) == (i & 1)) {
-              const uint2 ks = lds64(sb + (lane & 15) * kSlotBytes + kKScaleOff);
+        }
+        if (aborted) break;
+        tc_fence_after_sync();
+        // token k = 32 m + lane (tile 2m + lane/16): its largest V block byte
+        // E, the relative scales of blocks 2cq and 2cq+1, and (for this
+        // quarter's own tokens, m == cq) the V exponent and the K scale bytes
+        uint32_t sfw0 = 0, sfw1 = 0;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const bool hi = lane >= 16;
+          const int nvt = hi ? nv[2 * m + 1] : nv[2 * m];
+          const uint32_t row = (hi ? sb[2 * m + 1] : sb[2 * m]) + (lane & 15) * kSlotBytes;
+          uint32_t f = 0u, E = 0u;
+          if (nvt > 0) {
+            const uint2 sc = ld64(row + kVScaleOff);
+            E = max_byte8(sc.x, sc.y);
+            const uint32_t w = cq < 2 ? sc.x : sc.y;
+            f = pow2_rel_f16x2((E - ((w >> vsh) & 0xffu)) | ((E - ((w >> (vsh + 8)) & 0xffu)) << 16));
+            if (m == cq) {
+              const uint2 ks = ld64(row + kKScaleOff);
               sfw0 = ks.x;
               sfw1 = ks.y;
             }
-            __syncwarp();
-            // V: tokens 2c, 2c+1 (pair A) and 2c+8, 2c+9 (pair B), head dims
-            // 64cq + 8gq .. +7; the same dim of a pair shares one byte
-            const uint32_t x0 = lds32(sb + (2 * c) * kSlotBytes + voff);
-            const uint32_t x1 = lds32(sb + (2 * c + 1) * kSlotBytes + voff);
-            const uint32_t x2 = lds32(sb + (2 * c + 8) * kSlotBytes + voff);
-            const uint32_t x3 = lds32(sb + (2 * c + 9) * kSlotBytes + voff);
-            const uint32_t rvA = __byte_perm(lds32(meta + 8 * c), lds32(meta + 8 * c + 4), half_sel);
-            const uint32_t rvB = __byte_perm(lds32(meta + 8 * c + 32), lds32(meta + 8 * c + 36), half_sel);
-            uint32_t LA[4], HA[4], LB[4], HB[4];
+          }
+          st32(meta + 4 * (32 * m + lane), f);
+          if (m == cq)
+            st32(sbase + Lay::kEvfOff + (buf * kGroupTokens + 32 * m + lane) * 4,
+                  __float_as_uint(nvt > 0 ? (float)((int)E - 127 - kRelTop) : 0.f));
+        }
+#pragma unroll
+        for (int i = 0; i < kGroupTiles; ++i)
+          if ((i >> 1) == cq && lane == (i & 1)) st32(sbase + Lay::kGnvOff + (buf * kGroupTiles + i) * 4, (uint32_t)nv[i]);
+        __syncwarp();
+        // V: tokens 2c, 2c+1 (pair A) and 2c+8, 2c+9 (pair B) of each tile,
+        // head dims 64cq + 8gq .. +7; the same dim of a pair shares one byte
+#pragma unroll
+        for (int i = 0; i < kGroupTiles; ++i) {
+          const uint32_t vt = tmem + lane_q + Lay::kTmVt + 64 * (2 * buf) + 8 * i;
+          uint32_t LA[4] = {0u, 0u, 0u, 0u}, HA[4] = {0u, 0u, 0u, 0u}, LB[4] = {0u, 0u, 0u, 0u},
+                   HB[4] = {0u, 0u, 0u, 0u};
+          if (nv[i] > 0) {
+            const uint32_t x0 = ld32(sb[i] + (2 * c) * kSlotBytes + voff);
+            const uint32_t x1 = ld32(sb[i] + (2 * c + 1) * kSlotBytes + voff);
+            const uint32_t x2 = ld32(sb[i] + (2 * c + 8) * kSlotBytes + voff);
+            const uint32_t x3 = ld32(sb[i] + (2 * c + 9) * kSlotBytes + voff);
+            const uint32_t mt = meta + 4 * (16 * i + 2 * c);
+            const uint32_t rvA = __byte_perm(ld32(mt), ld32(mt + 4), half_sel);
+            const uint32_t rvB = __byte_perm(ld32(mt + 32), ld32(mt + 36), half_sel);
             f16x2x4_from_e2m1_word((x0 & 0x0F0F0F0Fu) | ((x1 << 4) & 0xF0F0F0F0u), LA);
             f16x2x4_from_e2m1_word(((x0 >> 4) & 0x0F0F0F0Fu) | (x1 & 0xF0F0F0F0u), HA);
             f16x2x4_from_e2m1_word((x2 & 0x0F0F0F0Fu) | ((x3 << 4) & 0xF0F0F0F0u), LB);
@@ -449,42 +543,40 @@ decode_stage1_wide(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_s
               LB[e] = hmul2(LB[e], rvB);
               HB[e] = hmul2(HB[e], rvB);
             }
-            // half h, m-tile mt: dims 8gq + 4h + 2mt (+1) at lanes 16mt + gq (+8)
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-              for (int mt = 0; mt < 2; ++mt)
-                tmem_st_16x128b_x2(vt + ((uint32_t)(16 * mt) << 16) + 64 * h, LA[2 * h + mt], HA[2 * h + mt],
-                                   LB[2 * h + mt], HB[2 * h + mt]);
-            if (mine) {
-              // K codes of the 16 tokens into rows 16i .. 16i+15 of the K operand
-              const uint32_t ka = sbase + Lay::kKaOff + buf * kKaBytes;
-#pragma unroll
-              for (int rep = 0; rep < 4; ++rep) {
-                const int idx = rep * 32 + lane, t = idx & 15, m = idx >> 4;   // token fastest
-                const uint4 v = lds128(sb + t * kSlotBytes + 16 * m);
-                const int row = 16 * i + t;
-                const uint32_t base = ka + (row >> 3) * 128 + (row & 7) * 16;
-                sts128(base + (2 * m) * kKaChunk, make_uint4(v.x, v.y, 0u, 0u));
-                sts128(base + (2 * m + 1) * kKaChunk, make_uint4(v.z, v.w, 0u, 0u));
-              }
-            }
-          } else {
-            // a missing or rejected tile: finite zeros in the PV operand
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-              for (int mt = 0; mt < 2; ++mt) tmem_st_16x128b_x2(vt + ((uint32_t)(16 * mt) << 16) + 64 * h, 0u, 0u, 0u, 0u);
-            if (mine && lane < 16) sts32(sbase + Lay::kEvfOff + (buf * kGroupTokens + 16 * i + lane) * 4, 0u);
           }
-          if (mine && lane == 0) sts32(sbase + Lay::kGnvOff + (buf * kGroupTiles + i) * 4, (uint32_t)nv);
-          if (j < U.n_tiles) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(Lay::bEmpty + slot));
-            ++tc;
+          // half h, m-tile mt: dims 8gq + 4h + 2mt (+1) at lanes 16mt + gq (+8);
+          // a missing or rejected tile leaves finite zeros
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+              tmem_st_16x128b_x2(vt + ((uint32_t)(16 * mt) << 16) + 64 * h, LA[2 * h + mt], HA[2 * h + mt],
+                                 LB[2 * h + mt], HB[2 * h + mt]);
+        }
+        // K codes of this quarter's tiles 2cq, 2cq+1 into rows 32cq .. 32cq+31
+        // of the K operand (16-element chunks of 8 code bytes and 8 unused)
+        const uint32_t ka = sbase + Lay::kKaOff + buf * kKaBytes;
+#pragma unroll
+        for (int i = 0; i < kGroupTiles; ++i) {
+          if ((i >> 1) == cq && nv[i] > 0) {
+            // all four loads before any store: the stores could alias them
+            // as far as the compiler knows
+            uint4 v[4];
+#pragma unroll
+            for (int rep = 0; rep < 4; ++rep) {
+              const int idx = rep * 32 + lane, t = idx & 15, m = idx >> 4;   // token fastest
+              v[rep] = ld128(sb[i] + t * kSlotBytes + 16 * m);
+            }
+#pragma unroll
+            for (int rep = 0; rep < 4; ++rep) {
+              const int idx = rep * 32 + lane, t = idx & 15, m = idx >> 4;
+              const int row = 16 * i + t;
+              const uint32_t base = ka + (row >> 3) * 128 + (row & 7) * 16;
+              st128(base + (2 * m) * kKaChunk, make_uint4(v[rep].x, v[rep].y, 0u, 0u));
+              st128(base + (2 * m + 1) * kKaChunk, make_uint4(v[rep].z, v[rep].w, 0u, 0u));
+            }
           }
         }
-        if (aborted) break;
         // K scales of the quarter's 32 token lanes: blocks 0-3 in column +0,
         // blocks 4-7 in column +4 (one byte per block)
         const uint32_t sfv[8] = {sfw0, sfw0, sfw0, sfw0, sfw1, sfw1, sfw1, sfw1};
@@ -493,7 +585,13 @@ decode_stage1_wide(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_s
         fence_proxy_async_smem();
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(Lay::bConv + buf));
+        if (lane == 0) {
+          mbar_arrive(bar(Lay::bConv + buf));
+#pragma unroll
+          for (int i = 0; i < kGroupTiles; ++i)
+            if (i < n_here) mbar_arrive(bar(Lay::bEmpty + (tc + (uint32_t)i) % KST));
+        }
+        tc += (uint32_t)n_here;
         ++gc;
       }
       if (aborted) break;
@@ -618,118 +716,101 @@ decode_stage1_wide(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_s
         const int t_abs = g0 + t;
         const float ev = reinterpret_cast<const float*>(smem + Lay::kEvfOff)[buf * kGroupTokens + t];
         const bool masks = g0 < full_lo || g0 + kGroupTokens > full_hi;
-        // 16 scores of rows c0 .. c0+15 for this token, masked (scores stay in
-        // tensor memory; each pass reads the columns it needs)
-        auto scores16 = [&](int c0, float (&v)[16]) {
-          tmem_ld16(s_col + c0, v);
+        const uint32_t pb = sbase + Lay::kPbOff + buf * Lay::kPbBytes + t * 16;
+        // rows in chunks of up to 32: one tensor-memory load each, the scores
+        // then stay in registers for the vote, the rare update and the weights
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            bool ok = tok_ok;
-            if (masks) ok = ok && t_abs >= s_rlo[c0 + k] && t_abs < s_rhi[c0 + k];
-            v[k] = ok ? v[k] * scale_log2e : -INFINITY;
+        for (int c0 = 0; c0 < NR; c0 += kChunk) {
+          float sv[kChunk];
+          tmem_ld_cols(s_col + c0, sv);
+#pragma unroll
+          for (int k = 0; k < kChunk; ++k) {
+            bool okk = tok_ok;
+            if (masks) okk = okk && t_abs >= s_rlo[c0 + k] && t_abs < s_rhi[c0 + k];
+            sv[k] = okk ? sv[k] * scale_log2e : -INFINITY;
           }
-        };
-        bool grow = false;
+          bool grow = false;
 #pragma unroll
-        for (int c0 = 0; c0 < NR; c0 += 16) {
-          float v[16];
-          scores16(c0, v);
-#pragma unroll
-          for (int r0 = 0; r0 < 16; r0 += 4) {
+          for (int r0 = 0; r0 < kChunk; r0 += 4) {
             const float4 m4 = *reinterpret_cast<const float4*>(s_m + c0 + r0);
             const float4 d4 = *reinterpret_cast<const float4*>(s_d + c0 + r0);
             const float mm[4] = {m4.x, m4.y, m4.z, m4.w}, dd[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const float sc = v[r0 + k];
+              const float sc = sv[r0 + k];
               const float m_ref = mm[k] == -INFINITY ? 0.f : mm[k];
               grow |= sc > mm[k] + kLazyMaxLog2;
               grow |= (sc - m_ref) + ev > dd[k] + kLazyMaxLog2;
             }
           }
-        }
-        if (bar_or_named(kSoftBar, kSoftThreads, grow)) {
-          // rare: new running maxima.  1) the group's row maxima of s
+          if (bar_or_named(kSoftBar, kSoftThreads, grow)) {
+            // rare: new running maxima for the chunk's rows.  1) the group's
+            // row maxima of s
 #pragma unroll
-          for (int c0 = 0; c0 < NR; c0 += 16) {
-            float v[16];
-            scores16(c0, v);
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              float x = v[k];
+            for (int k = 0; k < kChunk; ++k) {
+              float x = sv[k];
 #pragma unroll
               for (int msk = 1; msk < 32; msk <<= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, msk));
               if (lane == 0) red[(sq * 2) * NR + c0 + k] = x;
             }
-          }
-          bar_sync_named(kSoftBar, kSoftThreads);
-          // 2) the new m, and the maxima of the V exponents relative to it
+            bar_sync_named(kSoftBar, kSoftThreads);
+            // 2) the new m, and the maxima of the V exponents relative to it
 #pragma unroll
-          for (int c0 = 0; c0 < NR; c0 += 16) {
-            float v[16];
-            scores16(c0, v);
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
+            for (int k = 0; k < kChunk; ++k) {
               const int r = c0 + k;
               const float tm = fmaxf(fmaxf(red[0 * NR + r], red[2 * NR + r]), fmaxf(red[4 * NR + r], red[6 * NR + r]));
               const float m_old = s_m[r];
               const float m_new = tm > m_old + kLazyMaxLog2 ? tm : m_old;
               if (m_new != m_old) lp[r] *= fast_exp2(m_old - m_new);
               const float m_ref = m_new == -INFINITY ? 0.f : m_new;
-              float y = (v[k] - m_ref) + ev;
+              float y = (sv[k] - m_ref) + ev;
 #pragma unroll
               for (int msk = 1; msk < 32; msk <<= 1) y = fmaxf(y, __shfl_xor_sync(0xffffffffu, y, msk));
               if (lane == 0) red[(sq * 2 + 1) * NR + r] = y;
             }
-          }
-          bar_sync_named(kSoftBar, kSoftThreads);
-          // 3) one thread per row moves the state; fac = O's factor
-          bool moved = false;
-          if (st < NR) {
-            const int r = st;
-            const float tm = fmaxf(fmaxf(red[0 * NR + r], red[2 * NR + r]), fmaxf(red[4 * NR + r], red[6 * NR + r]));
-            const float ym = fmaxf(fmaxf(red[1 * NR + r], red[3 * NR + r]), fmaxf(red[5 * NR + r], red[7 * NR + r]));
-            const float m_old = s_m[r], d_old = s_d[r];
-            const float m_new = tm > m_old + kLazyMaxLog2 ? tm : m_old;
-            const float d_cur = m_old == -INFINITY ? -INFINITY : d_old + (m_old - m_new);
-            const float d_new = ym > d_cur + kLazyMaxLog2 ? ym : d_cur;
-            fac[r] = d_new == d_cur ? 1.f : fast_exp2(d_cur - d_new);
-            moved = d_new != d_cur;
-            s_m[r] = m_new;
-            s_d[r] = d_new;
-          }
-          const bool resc = bar_or_named(kSoftBar, kSoftThreads, moved);   // also publishes s_m, s_d, fac
-          if (resc && grp > 0) {
-            // O^T holds the groups so far: wait for the last one's PV, then
-            // scale each row's column by its factor
-            const uint32_t pg = cg - 1;
-            const bool okr = wait_warp(bar(Lay::bPvDone + (pg & 1u)), (pg >> 1) & 1u, abort_flag, err);
-            if (bar_or_named(kSoftBar, kSoftThreads, !okr)) {
-              aborted = true;
-              break;
+            bar_sync_named(kSoftBar, kSoftThreads);
+            // 3) one thread per row moves the state; fac = O's factor
+            bool moved = false;
+            if (st < kChunk) {
+              const int r = c0 + st;
+              const float tm = fmaxf(fmaxf(red[0 * NR + r], red[2 * NR + r]), fmaxf(red[4 * NR + r], red[6 * NR + r]));
+              const float ym = fmaxf(fmaxf(red[1 * NR + r], red[3 * NR + r]), fmaxf(red[5 * NR + r], red[7 * NR + r]));
+              const float m_old = s_m[r], d_old = s_d[r];
+              const float m_new = tm > m_old + kLazyMaxLog2 ? tm : m_old;
+              const float d_cur = m_old == -INFINITY ? -INFINITY : d_old + (m_old - m_new);
+              const float d_new = ym > d_cur + kLazyMaxLog2 ? ym : d_cur;
+              fac[r] = d_new == d_cur ? 1.f : fast_exp2(d_cur - d_new);
+              moved = d_new != d_cur;
+              s_m[r] = m_new;
+              s_d[r] = d_new;
             }
-            tc_fence_after_sync();
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-              for (int r0 = 0; r0 < NR; r0 += 16) {
-                float o[16];
-                tmem_ld16(tmem + lane_q + Lay::kTmO + h * NR + r0, o);
-#pragma unroll
-                for (int k = 0; k < 16; ++k) o[k] *= fac[r0 + k];
-                tmem_st16(tmem + lane_q + Lay::kTmO + h * NR + r0, o);
+            const bool resc = bar_or_named(kSoftBar, kSoftThreads, moved);   // also publishes s_m, s_d, fac
+            if (resc && grp > 0) {
+              // O^T holds the groups so far: wait for the last one's PV, then
+              // scale the chunk rows' columns by their factors
+              const uint32_t pg = cg - 1;
+              const bool okr = wait_warp(bar(Lay::bPvDone + (pg & 1u)), (pg >> 1) & 1u, abort_flag, err);
+              if (bar_or_named(kSoftBar, kSoftThreads, !okr)) {
+                aborted = true;
+                break;
               }
-            tmem_wait_st();
+              tc_fence_after_sync();
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int r0 = 0; r0 < kChunk; r0 += 16) {
+                  float o[16];
+                  tmem_ld16(tmem + lane_q + Lay::kTmO + h * NR + c0 + r0, o);
+#pragma unroll
+                  for (int k = 0; k < 16; ++k) o[k] *= fac[c0 + r0 + k];
+                  tmem_st16(tmem + lane_q + Lay::kTmO + h * NR + c0 + r0, o);
+                }
+              tmem_wait_st();
+            }
           }
-        }
-        // probabilities: l and the f16 PV weights, P^T rows-contiguous per token
-        const uint32_t pb = sbase + Lay::kPbOff + buf * Lay::kPbBytes + t * 16;
+          // probabilities: l and the f16 PV weights, P^T rows-contiguous per token
 #pragma unroll
-        for (int c0 = 0; c0 < NR; c0 += 16) {
-          float v[16];
-          scores16(c0, v);
-#pragma unroll
-          for (int r8 = 0; r8 < 16; r8 += 8) {
+          for (int r8 = 0; r8 < kChunk; r8 += 8) {
             uint32_t pk[4];
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
@@ -742,7 +823,7 @@ decode_stage1_wide(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_s
               for (int k = 0; k < 4; ++k) {
                 const float m_ref = mm[k] == -INFINITY ? 0.f : mm[k];
                 const float d_ref = dd[k] == -INFINITY ? 0.f : dd[k];
-                const float x = v[r0 + k] - m_ref;
+                const float x = sv[r0 + k] - m_ref;
                 lp[c0 + r0 + k] += fast_exp2(x);
                 wv[k] = fast_exp2((x + ev) - d_ref);
               }
@@ -752,6 +833,7 @@ decode_stage1_wide(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_s
             sts128(pb + ((c0 + r8) >> 3) * kPbNGroup, make_uint4(pk[0], pk[1], pk[2], pk[3]));
           }
         }
+        if (aborted) break;
         tc_fence_before_sync();
         fence_proxy_async_smem();
         __syncwarp();

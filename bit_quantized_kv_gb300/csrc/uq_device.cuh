@@ -346,10 +346,13 @@ __device__ __forceinline__ void tmem_wait_st() {
 // (g = lane/4, c = lane%4) writes lane g columns c and c+4 (a, b) and lane
 // g+8 columns c and c+4 (c2, d) -- the A fragment of mma.m16n8k16, f16 pairs
 // along K, in one instruction (shape 16x128b, two repeats).
+// It touches no memory that the compiler tracks, so ordinary loads and stores
+// may be scheduled across it; it keeps its place among the other tcgen05
+// statements (all volatile), and tcgen05.wait::st completes it.
 __device__ __forceinline__ void tmem_st_16x128b_x2(uint32_t taddr, uint32_t a, uint32_t c2, uint32_t b,
                                                    uint32_t d) {
   asm volatile("tcgen05.st.sync.aligned.16x128b.x2.b32 [%0], {%1,%2,%3,%4};"
-               :: "r"(taddr), "r"(a), "r"(c2), "r"(b), "r"(d) : "memory");
+               :: "r"(taddr), "r"(a), "r"(c2), "r"(b), "r"(d));
 }
 
 // 8 consecutive 32-bit columns of the thread's own lane.
