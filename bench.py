@@ -391,7 +391,7 @@ def measure_decode(args, wl, dev, stream, peak, peak_kind, local, world):
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": _traffic_from_profile(wl.name),
                      "stage1_ms": round(s1_ms, 5), "stage1_bytes": kv_bytes},
-        "gpu_launches": n * 4,   # per step: store, plan, stage 1, stage 2
+        "gpu_launches": n * 5,   # per step: store, plan, stage 1, exact pass, stage 2
         "clocks": clocks.summary(),
     }
     return line, st
@@ -602,7 +602,7 @@ def run_gpu_mq(args, rank, local, world, dev, stream, peak, peak_kind, cpu=True)
                          "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
                          "frac": round(ach / peak, 4), "traffic": _traffic_from_profile("mq"),
                          "stage1_ms": round(statistics.mean(ms1), 5)},
-            "gpu_launches": args.steps * 3, "clocks": clocks.summary(),
+            "gpu_launches": args.steps * 4, "clocks": clocks.summary(),
             **({} if (rank != 0 or not cpu or args.no_cpu_baseline) else {"cpu_baseline": _mq_cpu_baseline(args.cpu_budget)})}
 
 

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libuq.so")
 
-SOURCES = ["uq_api.cu", "uq_store.cu", "uq_decode.cu", "uq_decode_wide.cu", "uq_dequant.cu", "uq_noalloc.cu"]
+SOURCES = ["uq_api.cu", "uq_store.cu", "uq_decode.cu", "uq_dequant.cu", "uq_noalloc.cu"]
 HEADERS = ["uq_device.cuh", "uq_decode_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",

@@ -374,11 +374,10 @@ uq_status uq_decode_multi_query(const void* query, const void* kv_cache, const i
     return fail(UQ_ERR_INVALID_ARG, "cached_len %d + q_len %d exceeds the %d pages of block_table",
                 cached_len, q_len, max_blocks_per_seq);
   if (sinks && !aligned(sinks, 4)) return fail(UQ_ERR_INVALID_ARG, "sinks must be 4-byte aligned");
-  // Consecutive chunk positions share a work unit, up to 64 query rows
-  // (8 positions of 8 query heads per kv head, 10 of 6, 4 of 16): each page
-  // is read and dequantised once for all of them.
-  const int max_rows = uq::kWideKernel ? 64 : 16;
-  const int pack = q_len > 1 ? (max_rows / (Hq / Hk) < q_len ? max_rows / (Hq / Hk) : q_len) : 1;
+  // Two consecutive chunk positions share a work unit when that makes at most
+  // 16 query rows (6 or 8 query heads per kv head): each page is read and
+  // dequantised once for both.
+  const int pack = (q_len > 1 && 2 * (Hq / Hk) <= 16) ? 2 : 1;
   const uq::SeqRows rows{nullptr, 0, cached_len, sliding_window, log2_tiles_per_page(block_size),
                          max_blocks_per_seq * (block_size / 16), pack, q_len};
   return launch_checked_decode(query, kv_cache, block_table, rows, scale, sinks, max_num_kv_splits,

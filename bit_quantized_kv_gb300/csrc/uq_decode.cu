@@ -142,6 +142,7 @@ decode_plan(const SeqRows rows, int B, int Hk, int S,
     if (tid == 0) {
       ws.hdr[0] = total;
       ws.hdr[1] = 0;
+      ws.hdr[2] = 0;
     }
     return;
   }
@@ -193,71 +194,174 @@ decode_plan(const SeqRows rows, int B, int Hk, int S,
   if (tid == kPlanThreads - 1) {
     ws.hdr[0] = off;   // the last thread's range ends the list
     ws.hdr[1] = 0;
+    ws.hdr[2] = 0;
   }
 }
 
 // ---------------------------------------------------------------------------
 // Stage 1.
 // ---------------------------------------------------------------------------
-// Exact score contribution of K blocks more than 2^27 below their token's
-// largest block, which the tensor-core pass leaves out (their f16 relative
-// scale would not be exact).  Such spreads never come out of a rotated K in
-// practice; the path exists so that scores stay exact for every cache the
-// store can write.  Lane (gq, c) computes, for tokens gq and gq + 8 of the
-// tile at sb and its score rows nt*8 + 2c + h, the sum over those blocks of
-// 2^(byte - 127) * sum_d E2M1(code_d) * q'[row][d], times scale*log2e, in
-// fp32, and stores it at dst as [nt][h][token] floats.  q' is read back from
-// the operand-order query rows (row stride q_row_bytes: head dim d sits in
-// k-step (d % 64) / 4 at f16 position 2 (d / 64) + (d & 1) + 8 ((d >> 1) & 1)).
-// Out of line and through shared memory, so that the rare path costs the
-// main loop no registers.
-template <int NT>
-__device__ __noinline__ void far_k_blocks(uint32_t sb, uint32_t q_base, int q_row_bytes, int gq, int c,
-                                          float scale_log2e, uint32_t dst) {
+// q' = f16(e4m3(q H / 16)) for one query row (bf16, 256 head dims) by one
+// warp: lane loads head dims 8*lane .. 8*lane+7, the Walsh-Hadamard butterflies
+// run in registers (strides 1..4) and across lanes (strides 8..128), and the
+// lane returns its 8 dims as four f16x2 (the lower dim in the low half).
+__device__ __forceinline__ void query_prime8(const uint16_t* __restrict__ q_row, int lane, uint32_t (&pk)[4]) {
+  const uint4 raw = *reinterpret_cast<const uint4*>(q_row + lane * 8);
+  float x[8];
+  const uint32_t uu[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-  for (int tt = 0; tt < 2; ++tt) {
-    const uint32_t slot = sb + (gq + 8 * tt) * kSlotBytes;
-    const uint2 sc = lds64(slot + kKScaleOff);
-    const uint32_t E = max_byte8(sc.x, sc.y);
-    float add[NT][2];
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = bf16_bits_to_f32(uu[i] & 0xffffu);
+    x[2 * i + 1] = bf16_bits_to_f32(uu[i] >> 16);
+  }
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) add[nt][0] = add[nt][1] = 0.f;
+  for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if ((i & h) == 0) {
+        const float a = x[i], cc = x[i + h];
+        x[i] = a + cc;
+        x[i + h] = a - cc;
+      }
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const float sgn = (lane & m) ? -1.f : 1.f;   // upper lane: other - own
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float other = __shfl_xor_sync(0xffffffffu, x[i], m);
+      x[i] = fmaf(x[i], sgn, other);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) pk[i] = e4m3_roundtrip_f16x2(x[2 * i] * 0.0625f, x[2 * i + 1] * 0.0625f);
+}
+
+// 2^e as fp32 for an integer e <= 0 (subnormal below -126, 0 below -149).
+__device__ __forceinline__ float pow2_nonpos(int e) {
+  return e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23)
+                   : (e >= -149 ? __uint_as_float(1u << (e + 149)) : 0.f);
+}
+
+// The exact pass over the pages of a work unit, for units that hold a token
+// whose K blocks span 2^28 or more: the tensor-core pass keeps K block scales
+// relative to the token's largest block as f16 and cannot hold such a block
+// exactly.  Such spreads do not come out of a rotated K in practice; the pass
+// exists so that scores stay exact for every cache the store can write.
+// Everything here is plain fp32 on the CUDA cores, read straight from the
+// cache in global memory: score s = scale*log2e * sum over blocks of
+// 2^(byte - 127) * (E2M1 codes . q'), then the same online softmax state as
+// the main loop -- m (running maximum), d (V reference relative to m), l (sum
+// of 2^(s - m)) -- with every update taken eagerly, and O accumulated with V
+// taken relative to its token's largest block (2^(byte - E_V)) and weight
+// 2^(s - m + E_V - 127 - d).
+// Lane (gq, c) computes K block gq's share of every score of rows
+// nt*8 + 2c + h (the 8 lanes of a row sum their shares), and accumulates O
+// for head dims 32gq .. 32gq+31 of those rows: acc[mt][k] holds row
+// nt*8 + 2c + (k & 1), head dim 32gq + 2mt + (k >> 1), the layout of the
+// stage-1 kernel's O fragments.  q_rows points at row nt*8 + 2c of q' (f16,
+// head dims in order, row stride q_row_bytes).  Returns the state of rows
+// nt*8 + 2c + h in m, d, l (l whole in lane gq == 0, 0 elsewhere, so that
+// the sum over the row's lanes is the row sum) and acc.
+template <bool GEN>
+__device__ __forceinline__ void exact_rows(const uint8_t* __restrict__ kv, const int32_t* __restrict__ bt_row,
+                                           int num_blocks, int Hk, int g, int lg_tpp, int page0, int n_my,
+                                           int page_step, int L, const int (&lo)[2], const int (&hi)[2],
+                                           const uint8_t* q_rows, int q_row_bytes, float scale_log2e, int gq,
+                                           float (&m)[2], float (&d)[2], float (&l)[2], float (&acc)[16][4]) {
+  const int tile_mask = (1 << lg_tpp) - 1;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    m[h] = -INFINITY;
+    d[h] = -INFINITY;
+    l[h] = 0.f;
+  }
+#pragma unroll
+  for (int mt = 0; mt < 16; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+  const int64_t tok_stride = (int64_t)Hk * kSlotBytes;
 #pragma unroll 1
-    for (int blk = 0; blk < 8; ++blk) {
-      const uint32_t e = ((blk < 4 ? sc.x : sc.y) >> (8 * (blk & 3))) & 0xffu;
-      if (E - e < kRelSpan) continue;
-      float acc[NT][2];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = 0.f;
+  for (int j = 0; j < n_my; ++j) {
+    const int page = page0 + j * page_step;
+    const int pid = bt_row[page >> lg_tpp];
+    if ((unsigned)pid >= (unsigned)num_blocks) continue;   // reported by the main loop
+    const int nval = min(kPage, L - page * kPage);
+    const uint8_t* tile = kv + ((int64_t)((pid << lg_tpp) + (page & tile_mask)) * kPage * Hk + g) * kSlotBytes;
 #pragma unroll 1
-      for (int w = 0; w < 4; ++w) {   // 8 head dims per code word
+    for (int t = 0; t < nval; ++t) {
+      const uint8_t* slot = tile + t * tok_stride;
+      const uint4 kc = *reinterpret_cast<const uint4*>(slot + 16 * gq);
+      const float kscale = scale_log2e * ue8m0_to_f32(slot[kKScaleOff + gq]);
+      const uint32_t kw[4] = {kc.x, kc.y, kc.z, kc.w};
+      float part[2] = {0.f, 0.f};
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
         uint32_t f[4];
-        f16x2x4_from_e2m1_word(lds32(slot + 16 * blk + 4 * w), f);
+        f16x2x4_from_e2m1_word(kw[w], f);
 #pragma unroll
         for (int e8 = 0; e8 < 8; ++e8) {
-          const float kv = __half2float(__ushort_as_half((unsigned short)(f[e8 >> 1] >> (16 * (e8 & 1)))));
-          const int d = 32 * blk + 8 * w + e8;
-          const uint32_t qoff = ((d & 63) >> 2) * 32 + 2 * (2 * (d >> 6) + (d & 1) + 8 * ((d >> 1) & 1));
+          const float kval = __half2float(__ushort_as_half((unsigned short)(f[e8 >> 1] >> (16 * (e8 & 1)))));
+          const int dim = 32 * gq + 8 * w + e8;
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const uint32_t qa = q_base + (nt * 8 + 2 * c + h) * q_row_bytes + qoff;
-              acc[nt][h] = fmaf(kv, __half2float(__ushort_as_half((unsigned short)lds16(qa))), acc[nt][h]);
-            }
+          for (int h = 0; h < 2; ++h) {
+            const uint16_t qb = *reinterpret_cast<const uint16_t*>(q_rows + h * q_row_bytes + 2 * dim);
+            part[h] = fmaf(kval, __half2float(__ushort_as_half(qb)), part[h]);
+          }
         }
       }
-      const float bscale = scale_log2e * ue8m0_to_f32(e);
+      float sc[2];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+      for (int h = 0; h < 2; ++h) {
+        float x = part[h] * kscale;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) add[nt][h] = fmaf(acc[nt][h], bscale, add[nt][h]);
+        for (int msk = 4; msk < 32; msk <<= 1) x += __shfl_xor_sync(0xffffffffu, x, msk);
+        sc[h] = x;
+      }
+      const uint2 vs = *reinterpret_cast<const uint2*>(slot + kVScaleOff);
+      const uint32_t Ev = max_byte8(vs.x, vs.y);
+      const uint32_t vb = ((gq < 4 ? vs.x : vs.y) >> (8 * (gq & 3))) & 0xffu;
+      const float vrel = pow2_nonpos((int)vb - (int)Ev);
+      const float ev = (float)((int)Ev - 127);
+      const uint4 vc = *reinterpret_cast<const uint4*>(slot + kVCodeOff + 16 * gq);
+      const uint32_t vw[4] = {vc.x, vc.y, vc.z, vc.w};
+      const int tok = page * kPage + t;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (GEN && (tok < lo[h] || tok >= hi[h])) continue;
+        const float sv = sc[h];
+        if (sv > m[h]) {
+          if (m[h] != -INFINITY) {
+            l[h] *= exp2f(m[h] - sv);
+            d[h] += m[h] - sv;
+          }
+          m[h] = sv;
+        }
+        const float u = (sv - m[h]) + ev;
+        if (u > d[h]) {
+          if (d[h] != -INFINITY) {
+            const float a = exp2f(d[h] - u);
+#pragma unroll
+            for (int mt = 0; mt < 16; ++mt) {
+              acc[mt][h] *= a;
+              acc[mt][2 + h] *= a;
+            }
+          }
+          d[h] = u;
+        }
+        l[h] += exp2f(sv - m[h]);
+        const float wt = exp2f(u - d[h]) * vrel;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          uint32_t f[4];
+          f16x2x4_from_e2m1_word(vw[w], f);
+#pragma unroll
+          for (int e8 = 0; e8 < 8; ++e8) {
+            const float vval = __half2float(__ushort_as_half((unsigned short)(f[e8 >> 1] >> (16 * (e8 & 1)))));
+            acc[4 * w + (e8 >> 1)][2 * (e8 & 1) + h] = fmaf(wt, vval, acc[4 * w + (e8 >> 1)][2 * (e8 & 1) + h]);
+          }
+        }
+      }
     }
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) sts32(dst + 4 * ((nt * 2 + h) * 2 + tt), __float_as_uint(add[nt][h]));
   }
+  if (gq != 0) l[0] = l[1] = 0.f;
 }
 
 template <int NT, int NWARPS, int NSTAGE>
@@ -279,12 +383,9 @@ struct Stage1Layout {
   static constexpr int kMetaRelBytes = 2 * kPage * 16;
   static constexpr int kMetaWarpBytes = kMetaRelBytes + 2 * kPage * 4;
   static constexpr int kMetaOff = (kRowInfoOff + kRowInfoBytes + 15) / 16 * 16;
-  // per lane: the far-K-block score additions of the rare exact path, [NT][2][2] floats
-  static constexpr int kFixOff = kMetaOff + NWARPS * kMetaWarpBytes;
-  static constexpr int kFixBytes = NWARPS * 32 * NT * 16;
-  static constexpr int kBarOff = kFixOff + kFixBytes;
+  static constexpr int kBarOff = kMetaOff + NWARPS * kMetaWarpBytes;
   static constexpr int kBarBytes = NWARPS * NSTAGE * 8;
-  static constexpr int kMiscOff = kBarOff + kBarBytes;       // unit id, abort flag, TMEM base
+  static constexpr int kMiscOff = kBarOff + kBarBytes;       // unit id, abort flag, TMEM base, redo flag
   static constexpr int kQOff = (kMiscOff + 16 + 127) / 128 * 128;
   static constexpr int kQRowBytes = kHeadDim * 2 + 16;       // padded: conflict-free ldmatrix
   static constexpr int kQBytes = kRows * kQRowBytes;
@@ -296,8 +397,8 @@ struct Stage1Layout {
 template <int NT, int NWARPS, int NSTAGE, bool GEN>
 __global__ void __launch_bounds__(NWARPS * 32, NT == 1 ? UQ_S1_MIN_BLOCKS : kTmemCtasPerSm)
 decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
-              const __grid_constant__ CUtensorMap kv_map, const int32_t* __restrict__ block_table,
-              const SeqRows rows, float scale_log2e, int Hq, int Hk,
+              const __grid_constant__ CUtensorMap kv_map, const uint8_t* __restrict__ kv,
+              const int32_t* __restrict__ block_table, const SeqRows rows, float scale_log2e, int Hq, int Hk,
               int QG, int num_blocks, int S, Workspace ws,
               unsigned* __restrict__ err) {
   using Lay = Stage1Layout<NT, NWARPS, NSTAGE>;
@@ -316,6 +417,7 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
   if (threadIdx.x == 0) {
     for (int i = 0; i < NWARPS * NSTAGE; ++i) mbar_init(smem_base + Lay::kBarOff + 8 * i, 1);
     s_misc[1] = 0;
+    s_misc[3] = 0;
     fence_barrier_init();
   }
   if constexpr (Lay::kTmemO) {
@@ -427,37 +529,8 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
     for (int r = warp; r < Lay::kRows; r += NWARPS) {
       uint8_t* row = reinterpret_cast<uint8_t*>(qs) + r * Lay::kQRowBytes;
       uint32_t pk[4] = {0u, 0u, 0u, 0u};
-      if (row_exists(r)) {
-        const uint16_t* qp = query + (int64_t)row_of(r) * q_ss + (int64_t)head_of(r) * q_sh + lane * 8;
-        const uint4 raw = *reinterpret_cast<const uint4*>(qp);
-        float x[8];
-        const uint32_t uu[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          x[2 * i] = bf16_bits_to_f32(uu[i] & 0xffffu);
-          x[2 * i + 1] = bf16_bits_to_f32(uu[i] >> 16);
-        }
-#pragma unroll
-        for (int h = 1; h < 8; h <<= 1)
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            if ((i & h) == 0) {
-              const float a = x[i], cc = x[i + h];
-              x[i] = a + cc;
-              x[i + h] = a - cc;
-            }
-#pragma unroll
-        for (int m = 1; m < 32; m <<= 1) {
-          const float sgn = (lane & m) ? -1.f : 1.f;   // upper lane: other - own
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float other = __shfl_xor_sync(0xffffffffu, x[i], m);
-            x[i] = fmaf(x[i], sgn, other);
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) pk[i] = e4m3_roundtrip_f16x2(x[2 * i] * 0.0625f, x[2 * i + 1] * 0.0625f);
-      }
+      if (row_exists(r))
+        query_prime8(query + (int64_t)row_of(r) * q_ss + (int64_t)head_of(r) * q_sh, lane, pk);
       // lane holds head dims 8*lane .. 8*lane+7: c' = lane / 8, k-steps 2(lane % 8) + {0, 1}
       const int cq = lane >> 3, i0 = 2 * (lane & 7);
 #pragma unroll
@@ -520,10 +593,10 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
         // -- tile metadata, one (token, K or V) scale row per lane: the token's
         //    largest block byte E, the 8 relative scales 2^(13 + byte - E) as
         //    f16 and one fp32 factor (K: scale*log2e*2^(E-127-13); V:
-        //    E-127-13).  A K block more than 2^27 below its token's largest
-        //    block gets a relative scale of 0 here and is added back exactly
-        //    by the fix-up below (need_fix, rare).
-        bool need_fix;
+        //    E-127-13).  A token with a K block 2^28 or more below its
+        //    largest block gets a NaN K factor instead: its scores, and so
+        //    this lane's running sum, turn NaN, and the merge below hands
+        //    the unit to the exact pass (rare).
         {
           const int mtok = lane & 15, kind = lane >> 4;
           const uint2 sc = lds64(sb + mtok * kSlotBytes + kKScaleOff + 8 * kind);
@@ -539,9 +612,10 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
           p[2] = pow2_rel_f16x2(__byte_perm(dy, 0, 0x4140));
           p[3] = pow2_rel_f16x2(__byte_perm(dy, 0, 0x4342));
           sts128(meta_rel + (kind * kPage + mtok) * 16, make_uint4(p[0], p[1], p[2], p[3]));
-          const float f = kind == 0 ? scale_log2e * ue8m0_rel_to_f32(E) : (float)((int)E - 127 - kRelTop);
+          const float f = kind != 0 ? (float)((int)E - 127 - kRelTop)
+                        : (any_rel_zero(p[0], p[1], p[2], p[3]) ? __uint_as_float(0x7fc00000u)
+                                                                 : scale_log2e * ue8m0_rel_to_f32(E));
           sts32(meta_f + (kind * kPage + mtok) * 4, __float_as_uint(f));
-          need_fix = __any_sync(0xffffffffu, kind == 0 && E - min_byte8(sc.x, sc.y) >= kRelSpan);
         }
         __syncwarp();
         // K relative scales of tokens gq, gq+8 for blocks 2c, 2c+1 as f16x2 (both halves)
@@ -629,16 +703,6 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
             sv[nt][h][0] = (GEN ? v0r[nt][h] : v0) ? sres[h] * fk0 : -INFINITY;
             sv[nt][h][1] = (GEN ? v1r[nt][h] : v1) ? sres[2 + h] * fk1 : -INFINITY;
           }
-        }
-        if (need_fix) {   // rare: K blocks beyond the f16 span, added exactly (masked entries stay -inf)
-          const uint32_t fx = smem_base + Lay::kFixOff + (warp * 32 + lane) * (NT * 16);
-          far_k_blocks<NT>(sb, smem_u32(qs), Lay::kQRowBytes, gq, c, scale_log2e, fx);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-              for (int tt = 0; tt < 2; ++tt) sv[nt][h][tt] += __uint_as_float(lds32(fx + 4 * ((nt * 2 + h) * 2 + tt)));
         }
         // With rows of different lengths in one unit (GEN), a row can meet a
         // page with none of its tokens before any page with one; its maximum
@@ -854,10 +918,13 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
       float M = -INFINITY;
       for (int w = 0; w < NWARPS; ++w) M = fmaxf(M, stats[(w * Lay::kRows + r) * 4]);
       float Ls = 0.f;
+      bool bad = false;   // a warp met a token beyond the f16 span: the exact pass redoes the unit
       for (int w = 0; w < NWARPS; ++w) {
         const float* st = stats + (w * Lay::kRows + r) * 4;
         if (st[2] > 0.f) Ls += st[2] * fast_exp2(st[0] - M);
+        bad |= isnan(st[2]);
       }
+      if (bad) s_misc[3] = 1;
       float* ri = rowinfo + r * (NWARPS + 2);
       for (int w = 0; w < NWARPS; ++w) {
         const float* st = stats + (w * Lay::kRows + r) * 4;
@@ -924,6 +991,10 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
       }
       __syncthreads();  // the merge buffer (the stage buffers) and Q' are free again
     }
+    if (threadIdx.x == 0 && s_misc[3]) {
+      ws.redo[atomicAdd(&ws.hdr[2], 1)] = (uint32_t)u;
+      s_misc[3] = 0;
+    }
   }
   if constexpr (Lay::kTmemO) {
     tmem_wait_st();
@@ -931,6 +1002,83 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
     __syncthreads();
     tc_fence_after_sync();
     if (warp == 0) tmem_dealloc((uint32_t)s_misc[2], kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The exact pass: the units that stage 1 listed for a redo (a token whose K
+// blocks span 2^28 or more) are recomputed in plain fp32, one warp per unit
+// over all of its pages, and their split partials are overwritten before
+// stage 2 merges them.  With an empty list every CTA returns at once.
+// ---------------------------------------------------------------------------
+constexpr int kExactWarps = 4;
+
+template <bool GEN>
+__global__ void __launch_bounds__(kExactWarps * 32)
+decode_exact_units(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh, const uint8_t* __restrict__ kv,
+                   const int32_t* __restrict__ block_table, const SeqRows rows, float scale_log2e, int Hq, int Hk,
+                   int QG, int num_blocks, int S, Workspace ws) {
+  __shared__ __align__(16) uint16_t q_all[kExactWarps][16][kHeadDim];   // q' of each warp's unit rows
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, c = lane & 3;
+  pdl_launch_dependents();
+  pdl_wait();   // stage 1's partials and redo list are complete
+  const int n = ws.hdr[2];
+  for (int i = blockIdx.x * kExactWarps + warp; i < n; i += gridDim.x * kExactWarps) {
+    const uint32_t unit = ws.units[ws.redo[i]];
+    const int b = (int)(unit & 0xffffu), split = (int)((unit >> 16) & 0xffu), g = (int)(unit >> 24);
+    // the unit's rows and pages, derived as in stage 1
+    const int L = GEN ? unit_len(rows, b) : row_len(rows, b);
+    const int P = (L + kPage - 1) / kPage;
+    const int lo = GEN ? unit_lo(rows, b) : 0;
+    const int pack = GEN ? rows.pack : 1;
+    const int last_row = GEN ? unit_last_row(rows, b) : b;
+    auto row_of = [&](int r) { return GEN ? min(b * pack + r / QG, last_row) : b; };
+    auto row_exists = [&](int r) { return GEN ? r < QG * pack && b * pack + r / QG <= last_row : r < QG; };
+    auto head_of = [&](int r) { return g * QG + (GEN ? r % QG : r); };
+    const int p_begin = lo / kPage + split * ws.seq_info[b].x;
+    const int p_end = min(p_begin + ws.seq_info[b].x, P);
+    const int out_rows = QG * pack;   // <= 16
+    uint16_t(*qw)[kHeadDim] = q_all[warp];
+    for (int r = 0; r < 16; ++r) {
+      uint32_t pk[4] = {0u, 0u, 0u, 0u};
+      if (r < out_rows && row_exists(r))
+        query_prime8(query + (int64_t)row_of(r) * q_ss + (int64_t)head_of(r) * q_sh, lane, pk);
+      *reinterpret_cast<uint4*>(&qw[r][8 * lane]) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+    __syncwarp();
+    const int32_t* bt_row = block_table + (int64_t)b * rows.bt_stride;
+    const int lg_tpp = GEN ? rows.lg_tpp : 0;
+    for (int nt = 0; nt * 8 < out_rows; ++nt) {
+      int rlo[2] = {0, 0}, rhi[2] = {L, L};
+      if constexpr (GEN) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          rhi[h] = row_len(rows, row_of(nt * 8 + 2 * c + h));
+          rlo[h] = row_lo(rows, rhi[h]);
+        }
+      }
+      float m[2], d[2], l[2], acc[16][4];
+      exact_rows<GEN>(kv, bt_row, num_blocks, Hk, g, lg_tpp, p_begin, p_end - p_begin, 1, L, rlo, rhi,
+                      reinterpret_cast<const uint8_t*>(&qw[nt * 8 + 2 * c][0]), kHeadDim * 2, scale_log2e, gq, m,
+                      d, l, acc);
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int msk = 4; msk < 32; msk <<= 1) l[h] += __shfl_xor_sync(0xffffffffu, l[h], msk);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int r = nt * 8 + 2 * c + h;
+        if (r >= out_rows || (GEN && !row_exists(r))) continue;
+        const int64_t orow = GEN ? (int64_t)row_of(r) * Hq + head_of(r) : (int64_t)(b * Hq + g * QG + r);
+        const float fac = l[h] > 0.f ? exp2f(d[h]) / l[h] : 0.f;
+        if (gq == 0) ws.part_lse[orow * S + split] = l[h] > 0.f ? m[h] + log2f(l[h]) : -INFINITY;
+        float* dst = ws.part_o + (orow * S + split) * kHeadDim + 32 * gq;
+#pragma unroll
+        for (int mt = 0; mt < 16; ++mt)
+          *reinterpret_cast<float2*>(dst + 2 * mt) = make_float2(acc[mt][h] * fac, acc[mt][2 + h] * fac);
+      }
+    }
+    __syncwarp();   // q_all[warp] is rewritten by the warp's next unit
   }
 }
 
@@ -1141,44 +1289,15 @@ static cudaError_t launch_plan_and_stage1(const uint16_t* query, int64_t q_ss, i
   if (e != cudaSuccess) return e;
   if (ev_before && (e = record_timing_event(ev_before, stream)) != cudaSuccess) return e;
   e = launch_overlapped(decode_stage1<NT, NWARPS, NSTAGE, GEN>, dim3(grid), dim3(NWARPS * 32), Lay::kBytes,
-                        stream, query, q_ss, q_sh, kv_map, bt, sl, scale * kLog2e, Hq, Hk, Hq / Hk,
+                        stream, query, q_ss, q_sh, kv_map, kv, bt, sl, scale * kLog2e, Hq, Hk, Hq / Hk,
                         num_blocks, S, ws, err);
   if (e != cudaSuccess) return e;
   if (ev_after && (e = record_timing_event(ev_after, stream)) != cudaSuccess) return e;
-  return cudaSuccess;
+  return launch_overlapped(decode_exact_units<GEN>, dim3((grid + 3) / 4), dim3(kExactWarps * 32), 0, stream, query,
+                           q_ss, q_sh, kv, bt, sl, scale * kLog2e, Hq, Hk, Hq / Hk, num_blocks, S, ws);
 }
 
 size_t decode_workspace_bytes(int B, int Hq, int S) { return workspace_bytes(B, Hq, S); }
-
-cudaError_t wide_stage1_grid(int rows_per_unit, int* grid);
-cudaError_t launch_wide_stage1(int rows_per_unit, const uint16_t* query, int64_t q_ss, int64_t q_sh,
-                               const CUtensorMap& kv_map, const int32_t* bt, const SeqRows& sl, float scale,
-                               int Hq, int Hk, int num_blocks, int S, const Workspace& ws, unsigned* err,
-                               cudaStream_t stream, int grid);
-
-// Plan, then the warp-specialised stage 1 for units of more than 8 query rows.
-static cudaError_t launch_plan_and_wide_stage1(const uint16_t* query, int64_t q_ss, int64_t q_sh,
-                                               const uint8_t* kv, const int32_t* bt, const SeqRows& sl,
-                                               float scale, int B, int Hq, int Hk, int num_blocks, int S,
-                                               const Workspace& ws, unsigned* err, cudaStream_t stream,
-                                               cudaEvent_t ev_before, cudaEvent_t ev_after) {
-  const int rows_per_unit = (Hq / Hk) * sl.pack;
-  int grid = 0;
-  cudaError_t e = wide_stage1_grid(rows_per_unit, &grid);
-  if (e != cudaSuccess) return e;
-  CUtensorMap kv_map;
-  const int64_t num_slots = (int64_t)num_blocks << (4 + sl.lg_tpp);
-  if ((e = make_kv_tensor_map(&kv_map, kv, Hk, num_slots)) != cudaSuccess) return e;
-  e = launch_overlapped(decode_plan, dim3(1), dim3(kPlanThreads), 0, stream, sl, (B + sl.pack - 1) / sl.pack, Hk,
-                        S, grid, kUnitCostTilesWide, ws);
-  if (e != cudaSuccess) return e;
-  if (ev_before && (e = record_timing_event(ev_before, stream)) != cudaSuccess) return e;
-  e = launch_wide_stage1(rows_per_unit, query, q_ss, q_sh, kv_map, bt, sl, scale, Hq, Hk, num_blocks, S, ws, err,
-                         stream, grid);
-  if (e != cudaSuccess) return e;
-  if (ev_after && (e = record_timing_event(ev_after, stream)) != cudaSuccess) return e;
-  return cudaSuccess;
-}
 
 cudaError_t launch_decode(const uint16_t* query, int64_t q_ss, int64_t q_sh, const uint8_t* kv,
                           const int32_t* bt, const SeqRows& sl, float scale, const float* sinks,
@@ -1187,7 +1306,7 @@ cudaError_t launch_decode(const uint16_t* query, int64_t q_ss, int64_t q_sh, con
                           cudaEvent_t ev_before_stage1, cudaEvent_t ev_after_stage1) {
   const Workspace ws = workspace_layout(workspace, B, Hq, S);
   const bool gen = sl.window > 0 || sl.lg_tpp > 0 || sl.pack > 1;
-  const bool wide = (Hq / Hk) * sl.pack > 8;
+  const bool sixteen = (Hq / Hk) * sl.pack > 8;
   auto run = [&](auto nt, auto g) {
     return launch_plan_and_stage1<decltype(nt)::value, decltype(g)::value>(
         query, q_ss, q_sh, kv, bt, sl, scale, B, Hq, Hk, num_blocks, max_blocks, S, ws, err, stream,
@@ -1197,14 +1316,8 @@ cudaError_t launch_decode(const uint16_t* query, int64_t q_ss, int64_t q_sh, con
   using Two = std::integral_constant<int, 2>;
   using Gen = std::true_type;
   using Plain = std::false_type;
-  cudaError_t e;
-  if (!wide)
-    e = gen ? run(One{}, Gen{}) : run(One{}, Plain{});
-  else if (kWideKernel)
-    e = launch_plan_and_wide_stage1(query, q_ss, q_sh, kv, bt, sl, scale, B, Hq, Hk, num_blocks, S, ws, err,
-                                    stream, ev_before_stage1, ev_after_stage1);
-  else
-    e = gen ? run(Two{}, Gen{}) : run(Two{}, Plain{});
+  cudaError_t e = sixteen ? (gen ? run(Two{}, Gen{}) : run(Two{}, Plain{}))
+                          : (gen ? run(One{}, Gen{}) : run(One{}, Plain{}));
   if (e != cudaSuccess) return e;
   const int rows = B * Hq;
   return launch_overlapped(decode_stage2, dim3((rows + 3) / 4), dim3(128), 0, stream, ws, B, Hq, S, sl.pack,

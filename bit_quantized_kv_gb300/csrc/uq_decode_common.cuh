@@ -33,17 +33,6 @@ constexpr int kTileBytes = kPage * kSlotBytes;   // 4352 bytes per (tile, kv hea
 constexpr int kMinPagesPerUnit = UQ_MIN_PAGES_PER_UNIT;  // floor of 128 tokens per split
 constexpr float kUnitCostTiles8 = UQ_UNIT_COST_TILES_8ROW;    // work units per CTA = sqrt(tiles / this)
 constexpr float kUnitCostTiles16 = UQ_UNIT_COST_TILES_16ROW;
-// Units of more than 8 rows: the warp-specialised tensor-core kernel (1), or
-// the 16-row mma.sync kernel with at most two query positions per unit (0).
-#ifndef UQ_WIDE_KERNEL
-#define UQ_WIDE_KERNEL 0
-#endif
-constexpr bool kWideKernel = UQ_WIDE_KERNEL != 0;
-// The warp-specialised kernel for units of 16 to 64 rows runs one CTA per SM.
-#ifndef UQ_UNIT_COST_TILES_WIDE
-#define UQ_UNIT_COST_TILES_WIDE 64
-#endif
-constexpr float kUnitCostTilesWide = UQ_UNIT_COST_TILES_WIDE;
 #ifndef UQ_MIN_UNITS_PER_CTA
 #define UQ_MIN_UNITS_PER_CTA 2
 #endif
@@ -72,7 +61,8 @@ struct Workspace {
   uint32_t* units;     // [<= S * B * Hk] b | split << 16 | kv_head << 24
   int2* seq_info;      // [B] (pages per split, active splits)
   int* order;          // [B] sequences with at least one page, longest split first
-  int* hdr;            // [0] number of units, [1] next unit to take
+  int* hdr;            // [0] number of units, [1] next unit to take, [2] units to redo
+  uint32_t* redo;      // [<= S * B * Hk] units whose stage-1 result needs the exact pass
 };
 
 __host__ __device__ inline size_t workspace_bytes(int B, int Hq, int S) {
@@ -97,6 +87,9 @@ __host__ __device__ inline Workspace workspace_layout(void* base, int B, int Hq,
   w.order = reinterpret_cast<int*>(p);
   p += (size_t)B * 4;
   w.hdr = reinterpret_cast<int*>(p);
+  // at most S * B * Hk <= rows / 6 units (6 or more query heads per kv
+  // head): the upper half of the units array holds the redo list
+  w.redo = w.units + rows / 2;
   return w;
 }
 

@@ -129,7 +129,7 @@ __device__ __forceinline__ float ue8m0_to_f32(uint32_t byte) {
 // packed as f16x2: the biased exponent 28 - d in bits 14..10 of each half.
 // A token's largest block (d = 0) maps to 2^13, so an E2M1 code times the
 // factor stays below 6 * 2^13 = 49152, inside f16's range.  d >= 28 gives +0:
-// a block more than 2^27 below its token's largest block is left to the
+// a block 2^28 or more below its token's largest block is left to the
 // caller; every kept factor is a normal f16, so the product c * 2^(13 - d)
 // of an E2M1 code c stays exact.
 constexpr uint32_t kRelSpan = 28;    // kept block exponents: d = 0 .. kRelSpan - 1
@@ -146,20 +146,27 @@ __device__ __forceinline__ float ue8m0_rel_to_f32(uint32_t byte) {
   return byte >= 14u ? __uint_as_float((byte - 13u) << 23) : __uint_as_float(1u << (byte + 9u));
 }
 
-// Largest of the eight bytes of (lo, hi).
+// Largest of the eight bytes of (lo, hi): the bytes spread over 16-bit
+// lanes (native lane-wise integer max), three lane-wise maxima, then the
+// larger lane.
 __device__ __forceinline__ uint32_t max_byte8(uint32_t lo, uint32_t hi) {
-  uint32_t m = __vmaxu4(lo, hi);
-  m = __vmaxu4(m, m >> 16);
-  m = __vmaxu4(m, m >> 8);
-  return m & 0xffu;
+  uint32_t m;
+  asm("{\n\t.reg .b32 a, b, c, d;\n\t"
+      "prmt.b32 a, %1, 0, 0x4240;\n\tprmt.b32 b, %1, 0, 0x4341;\n\t"
+      "prmt.b32 c, %2, 0, 0x4240;\n\tprmt.b32 d, %2, 0, 0x4341;\n\t"
+      "max.u16x2 a, a, b;\n\tmax.u16x2 c, c, d;\n\tmax.u16x2 %0, a, c;\n}\n"
+      : "=r"(m) : "r"(lo), "r"(hi));
+  return max(m & 0xffffu, m >> 16);
 }
 
-// Smallest of the eight bytes of (lo, hi).
-__device__ __forceinline__ uint32_t min_byte8(uint32_t lo, uint32_t hi) {
-  uint32_t m = __vminu4(lo, hi);
-  m = __vminu4(m, m >> 16);
-  m = __vminu4(m, m >> 8);
-  return m & 0xffu;
+// True if any of the eight halfwords of four f16x2 relative scales (from
+// pow2_rel_f16x2) is +0, i.e. some block lies 2^kRelSpan or more below its
+// token's largest block.
+__device__ __forceinline__ bool any_rel_zero(uint32_t p0, uint32_t p1, uint32_t p2, uint32_t p3) {
+  uint32_t m;
+  asm("{\n\t.reg .b32 t;\n\tmin.u16x2 t, %1, %2;\n\tmin.u16x2 %0, %3, %4;\n\tmin.u16x2 %0, %0, t;\n}\n"
+      : "=r"(m) : "r"(p0), "r"(p1), "r"(p2), "r"(p3));
+  return min(m & 0xffffu, m >> 16) == 0u;
 }
 
 // ---------------------------------------------------------------------------
@@ -337,100 +344,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
 
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-// ---------------------------------------------------------------------------
-// Shapes and forms used by the warp-specialised decode kernel.
-// ---------------------------------------------------------------------------
-// 16 lanes x 256 bits from registers in the mma.m16n8 fragment layout: thread
-// (g = lane/4, c = lane%4) writes lane g columns c and c+4 (a, b) and lane
-// g+8 columns c and c+4 (c2, d) -- the A fragment of mma.m16n8k16, f16 pairs
-// along K, in one instruction (shape 16x128b, two repeats).
-// It touches no memory that the compiler tracks, so ordinary loads and stores
-// may be scheduled across it; it keeps its place among the other tcgen05
-// statements (all volatile), and tcgen05.wait::st completes it.
-__device__ __forceinline__ void tmem_st_16x128b_x2(uint32_t taddr, uint32_t a, uint32_t c2, uint32_t b,
-                                                   uint32_t d) {
-  asm volatile("tcgen05.st.sync.aligned.16x128b.x2.b32 [%0], {%1,%2,%3,%4};"
-               :: "r"(taddr), "r"(a), "r"(c2), "r"(b), "r"(d));
-}
-
-// 8 consecutive 32-bit columns of the thread's own lane.
-__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&v)[8]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
-               :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
-                  "r"(v[7]) : "memory");
-}
-
-// 16 consecutive fp32 columns of the thread's own lane; valid on return.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  tmem_ld16_issue(taddr, v);
-  tmem_ld16_wait(v);
-}
-
-// Shared-memory matrix descriptor, no swizzle: the operand is stored as core
-// matrices of 8 rows x 16 bytes; `lbo` is the byte distance between core
-// matrices along K, `sbo` between core matrices along M (or N).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((saddr >> 4) & 0x3FFFu) | (uint64_t)((lbo >> 4) & 0x3FFFu) << 16 |
-         (uint64_t)((sbo >> 4) & 0x3FFFu) << 32 | (uint64_t)1 << 46;
-}
-
-// D (+)= (A x 2^sfa) (B x 2^sfb)^T with UE8M0 block scales, one 32-element
-// block of K per instruction (kind::mxf8f6f4, scale_vec 1X); A and B in
-// shared memory.
-__device__ __forceinline__ void tc_mma_block_scaled(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                                    uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
-                                                    uint32_t accumulate) {
-  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-               "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n\t}\n"
-               :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
-                  "r"(accumulate) : "memory");
-}
-
-// D (+)= A B^T, f16 operands, fp32 accumulators; A in tensor memory (M rows
-// along lanes, K along columns, two elements per 32-bit column), B in shared
-// memory.
-__device__ __forceinline__ void tc_mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                                  uint32_t idesc, uint32_t accumulate) {
-  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n"
-               :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
-}
-
-// Arrive once on `bar` when every tcgen05 operation this thread issued so
-// far has completed.
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-               :: "r"(bar) : "memory");
-}
-
-// Named barrier `id` over `count` threads (a multiple of 32), and its OR
-// reduction form.
-__device__ __forceinline__ void bar_sync_named(uint32_t id, uint32_t count) {
-  asm volatile("barrier.cta.sync %0, %1;" :: "r"(id), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ bool bar_or_named(uint32_t id, uint32_t count, bool pred) {
-  uint32_t r;
-  asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-               "barrier.cta.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n}\n"
-               : "=r"(r) : "r"((uint32_t)pred), "r"(id), "r"(count) : "memory");
-  return r != 0;
-}
-
-__device__ __forceinline__ void sts64(uint32_t addr, uint32_t a, uint32_t b) {
-  asm volatile("st.shared.v2.u32 [%0], {%1,%2};" :: "r"(addr), "r"(a), "r"(b) : "memory");
-}
-
-// Four fp32 -> four E4M3 bytes (round to nearest even, saturating at
-// +-448), `a` in the lowest byte.
-__device__ __forceinline__ uint32_t e4m3x4_from_f32(float a, float b, float c, float d) {
-  uint32_t r;
-  asm("{\n\t.reg .b16 lo, hi;\n\tcvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
-      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\tmov.b32 %0, {lo, hi};\n}\n"
-      : "=r"(r) : "f"(a), "f"(b), "f"(c), "f"(d));
-  return r;
 }
 
 }  // namespace uq

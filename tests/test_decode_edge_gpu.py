@@ -150,6 +150,61 @@ def test_k_block_spread(Hq, Hk, big_log2, n_big, window):
 
 
 @pytest.mark.parametrize("Hq,Hk", GROUPS)
+@pytest.mark.parametrize("every", [37, 400])
+def test_k_block_spread_on_some_tokens(Hq, Hk, every):
+    """Only every `every`-th token carries a K block at 2^40 (query rows zero
+    there): the units holding one are redone exactly, the others keep the
+    tensor-core result, and both kinds sit in one batch."""
+    rng = np.random.default_rng(1200 + every + Hq)
+    lens = [3, 700, 1500, 64]
+    wl = _layout(lens, Hq, Hk, seed=13, splits=6)
+    n = int(np.sum(lens))
+    kr = _rows(rng, n, Hk)
+    kr[5::every, :, 96:128] *= np.float32(2.0 ** 40)
+    vv = _rows(rng, n, Hk)
+    ref_cache = _fill(wl, kr, vv)
+    qp = rng.integers(-2, 3, size=(wl.B, Hq, D)).astype(np.float64)
+    qp[..., 96:128] = 0.0
+    q_bits = _query_from_prime(qp)
+    out = _decode(wl, ref_cache, q_bits)
+    compare(out, _oracle(wl, ref_cache, q_bits))
+
+
+@pytest.mark.parametrize("Hq,Hk,cached,q_len,block_size", [
+    (8, 1, 300, 5, 16),
+    (12, 2, 95, 3, 64),
+    (32, 2, 40, 4, 32),
+])
+def test_k_block_spread_multi_query(Hq, Hk, cached, q_len, block_size):
+    """K blocks at 2^40 on every token (query rows zero there) through the
+    multi-query entry and pages of more than 16 tokens: the exact pass redoes
+    the units with each chunk row's own causal range."""
+    rng = np.random.default_rng(1300 + cached + block_size)
+    L = cached + q_len
+    P = (L + block_size - 1) // block_size
+    S = 4
+    wl = workloads.make_decode_workload("edge_mq", 1, Hq, Hk, np.array([L]), P + 1, S, seed=14,
+                                        spare_blocks=2, block_size=block_size)
+    kr = _rows(rng, L, Hk)
+    kr[:, :, 0:32] *= np.float32(2.0 ** 40)
+    vv = _rows(rng, L, Hk)
+    ref_cache = _fill(wl, kr, vv)
+    qp = rng.integers(-2, 3, size=(q_len, Hq, D)).astype(np.float64)
+    qp[..., 0:32] = 0.0
+    q_bits = _query_from_prime(qp)
+    q = torch.from_numpy(q_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    cache = torch.from_numpy(ref_cache).cuda()
+    bt = torch.from_numpy(np.ascontiguousarray(wl.block_table[0])).cuda()
+    ws = torch.empty(binding.uq_decode_workspace_bytes(q_len, Hq, D, S), dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(q)
+    binding.uq_decode_multi_query(q, cache, bt, cached, wl.scale, S, ws, out)
+    assert binding.uq_check_device_error() == 0
+    table = np.tile(wl.block_table[0], (q_len, 1))
+    lens = (cached + 1 + np.arange(q_len)).astype(np.int32)
+    compare(out, oracle.decode(q_bits, ref_cache, table, lens, wl.scale))
+
+
+@pytest.mark.parametrize("Hq,Hk", GROUPS)
 @pytest.mark.parametrize("big_log2", [20, 60])
 def test_one_dominant_token_with_huge_scores(Hq, Hk, big_log2):
     """One token per sequence carries a K block at 2^big_log2 aligned with
