@@ -10,6 +10,11 @@
 
 namespace uq {
 
+// L2 sector promotion of the page copies (CUtensorMapL2promotion: 0 none,
+// 1 64 B, 2 128 B, 3 256 B).
+#ifndef UQ_KV_L2_PROMOTION
+#define UQ_KV_L2_PROMOTION 2
+#endif
 constexpr int kPage = 16;                        // tokens per tile (the smallest block_size)
 constexpr int kTileBytes = kPage * kSlotBytes;   // 4352 bytes per (tile, kv head)
 #ifndef UQ_MIN_PAGES_PER_UNIT
@@ -36,7 +41,10 @@ constexpr float kUnitCostTiles16 = UQ_UNIT_COST_TILES_16ROW;
 #ifndef UQ_MIN_UNITS_PER_CTA
 #define UQ_MIN_UNITS_PER_CTA 2
 #endif
-constexpr int kMinUnitsPerCta = UQ_MIN_UNITS_PER_CTA, kMaxUnitsPerCta = 8;
+#ifndef UQ_MAX_UNITS_PER_CTA
+#define UQ_MAX_UNITS_PER_CTA 8
+#endif
+constexpr int kMinUnitsPerCta = UQ_MIN_UNITS_PER_CTA, kMaxUnitsPerCta = UQ_MAX_UNITS_PER_CTA;
 constexpr int kStage1Stages = UQ_S1_NSTAGE;              // pages in flight per warp
 // 16-row query groups keep O^T (128 fp32 per lane) in tensor memory: 128
 // columns over all 128 lanes per CTA, each warp in its own 32 lanes.  That
