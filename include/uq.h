@@ -159,12 +159,18 @@ uq_status uq_store_rotated_f32(const float *key_rot, const float *value,
  * E4M3 "haircut", round to nearest even, saturating); s_t = scale * q'.k_t
  * over the L tokens of the sequence, k_t the dequantised rotated K;
  * out = softmax(s) . V (dequantised), rounded to bf16.  A sequence with
- * L == 0 gets out = 0.  Supported Hk <= 256, B <= 65535.  Three kernels run
+ * L == 0 gets out = 0.  Supported Hk <= 256, B <= 65535.  Four kernels run
  * on the stream: a one-CTA plan that divides every sequence into up to S
  * splits of whole pages (the split size is chosen on the device from the
  * batch's total length, so the work list has a few units per resident CTA)
  * and orders the units longest first; the split-KV kernel (persistent CTAs
- * taking units from that list); and the merge of each row's splits.
+ * taking units from that list); an exact fp32 pass over the units that hold
+ * a token whose K block scales span 2^28 or more (the split-KV kernel keeps
+ * K block scales relative to each token's largest one in f16 and lists such
+ * units instead; with no such token the pass returns at once); and the merge
+ * of each row's splits.  V blocks 2^28 or more below their token's largest
+ * V block are dropped by the split-KV kernel (each such value is below
+ * 6 * 2^-28 of that block in magnitude).
  */
 uq_status uq_decode(const void *query, const void *kv_cache,
                     const int32_t *block_table, const int32_t *seq_lens,
@@ -280,8 +286,9 @@ uq_status uq_full_dequant(const void *kv_cache, const int32_t *block_table, int 
  * A batch whose uq_decode_workspace_bytes(B, Hq, 256, max_num_kv_splits)
  * exceeds 32 MiB (roughly B * Hq * max_num_kv_splits > 32480) is rejected
  * with UQ_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.  The call allocates
- * nothing.  The first call on a device looks up the array's device address;
- * make that first call before any stream capture.  All calls on a device
+ * nothing.  The first call on a device (and the first after its CUDA
+ * context changes, e.g. after a device reset) looks up the array's device
+ * address; make that first call before any stream capture.  All calls on a device
  * share the one array, and it keeps the previous call's partials (nothing in
  * it needs to start at zero), so calls that can overlap on the GPU (for
  * example on two streams without an ordering between them) race.
