@@ -13,7 +13,7 @@ namespace uq {
 // L2 sector promotion of the page copies (CUtensorMapL2promotion: 0 none,
 // 1 64 B, 2 128 B, 3 256 B).
 #ifndef UQ_KV_L2_PROMOTION
-#define UQ_KV_L2_PROMOTION 2
+#define UQ_KV_L2_PROMOTION 1
 #endif
 constexpr int kPage = 16;                        // tokens per tile (the smallest block_size)
 constexpr int kTileBytes = kPage * kSlotBytes;   // 4352 bytes per (tile, kv head)
