@@ -395,7 +395,7 @@ struct Stage1Layout {
 // GEN: a sliding window or pages of more than 16 tokens.  The plain
 // instantiation (block_size 16, no window) folds both away.
 template <int NT, int NWARPS, int NSTAGE, bool GEN>
-__global__ void __launch_bounds__(NWARPS * 32, NT == 1 ? UQ_S1_MIN_BLOCKS : kTmemCtasPerSm)
+__global__ void __launch_bounds__(NWARPS * 32, NT == 1 ? UQ_S1_MIN_BLOCKS : (GEN ? kTmemCtasPerSmGen : kTmemCtasPerSm))
 decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
               const __grid_constant__ CUtensorMap kv_map, const uint8_t* __restrict__ kv,
               const int32_t* __restrict__ block_table, const SeqRows rows, float scale_log2e, int Hq, int Hk,
