@@ -141,7 +141,7 @@ decode_plan(const SeqRows rows, int B, int Hk, int S,
     }
     if (tid == 0) {
       ws.hdr[0] = total;
-      ws.hdr[1] = 0;
+      ws.hdr[1] = grid;   // units 0 .. grid-1 are each CTA's first
       ws.hdr[2] = 0;
     }
     return;
@@ -193,7 +193,7 @@ decode_plan(const SeqRows rows, int B, int Hk, int S,
   }
   if (tid == kPlanThreads - 1) {
     ws.hdr[0] = off;   // the last thread's range ends the list
-    ws.hdr[1] = 0;
+    ws.hdr[1] = grid;  // units 0 .. grid-1 are each CTA's first
     ws.hdr[2] = 0;
   }
 }
@@ -385,8 +385,9 @@ struct Stage1Layout {
   static constexpr int kMetaOff = (kRowInfoOff + kRowInfoBytes + 15) / 16 * 16;
   static constexpr int kBarOff = kMetaOff + NWARPS * kMetaWarpBytes;
   static constexpr int kBarBytes = NWARPS * NSTAGE * 8;
-  static constexpr int kMiscOff = kBarOff + kBarBytes;       // unit id, abort flag, TMEM base, redo flag
-  static constexpr int kQOff = (kMiscOff + 16 + 127) / 128 * 128;
+  // unit id, abort flag, TMEM base, redo flag, first unit taken
+  static constexpr int kMiscOff = kBarOff + kBarBytes;
+  static constexpr int kQOff = (kMiscOff + 32 + 127) / 128 * 128;
   static constexpr int kQRowBytes = kHeadDim * 2 + 16;       // padded: conflict-free ldmatrix
   static constexpr int kQBytes = kRows * kQRowBytes;
   static constexpr int kBytes = kQOff + kQBytes;
@@ -418,6 +419,7 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
     for (int i = 0; i < NWARPS * NSTAGE; ++i) mbar_init(smem_base + Lay::kBarOff + 8 * i, 1);
     s_misc[1] = 0;
     s_misc[3] = 0;
+    s_misc[4] = 0;
     fence_barrier_init();
   }
   if constexpr (Lay::kTmemO) {
@@ -441,7 +443,12 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
   const int ta = 2 * c, tb = 2 * c + 1, tcc = 2 * c + 8, td = 2 * c + 9;
 
   for (;;) {
-    if (threadIdx.x == 0) s_misc[0] = atomicAdd(&ws.hdr[1], 1);
+    // A CTA's first unit is its own index (the plan starts the counter at
+    // the grid size); later ones come from the counter.
+    if (threadIdx.x == 0) {
+      s_misc[0] = s_misc[4] ? atomicAdd(&ws.hdr[1], 1) : (int)blockIdx.x;
+      s_misc[4] = 1;
+    }
     __syncthreads();
     const int u = s_misc[0];
     if (u >= n_units || s_misc[1]) break;
