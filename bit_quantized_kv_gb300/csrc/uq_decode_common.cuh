@@ -61,7 +61,10 @@ constexpr int kTmemCtasPerSm = UQ_S1_NT2_MIN_BLOCKS;
 #define UQ_S1_NT2_GEN_MIN_BLOCKS 4
 #endif
 constexpr int kTmemCtasPerSmGen = UQ_S1_NT2_GEN_MIN_BLOCKS;
-constexpr int kPlanThreads = 1024;
+#ifndef UQ_PLAN_THREADS
+#define UQ_PLAN_THREADS 256
+#endif
+constexpr int kPlanThreads = UQ_PLAN_THREADS;
 constexpr float kLog2e = 1.4426950408889634f;
 // A running softmax maximum (log2 units) moves only when a page's maximum
 // exceeds it by more than this, so probabilities stay below 2^8.
