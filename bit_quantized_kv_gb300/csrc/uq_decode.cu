@@ -444,9 +444,11 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
 
   for (;;) {
     // A CTA's first unit is its own index (the plan starts the counter at
-    // the grid size); later ones come from the counter.
+    // the grid size); later ones come from the counter.  A CTA that gave up
+    // (its abort flag is set before the merge barriers) takes no more, so
+    // that no unit is taken and then left undone.
     if (threadIdx.x == 0) {
-      s_misc[0] = s_misc[4] ? atomicAdd(&ws.hdr[1], 1) : (int)blockIdx.x;
+      s_misc[0] = s_misc[1] ? n_units : (s_misc[4] ? atomicAdd(&ws.hdr[1], 1) : (int)blockIdx.x);
       s_misc[4] = 1;
     }
     __syncthreads();
