@@ -146,12 +146,6 @@ __device__ __forceinline__ int row_lo(const SeqRows& r, int L) {
   return (r.window > 0 && L > r.window) ? L - r.window : 0;
 }
 
-// Tiles a row reads: [row_lo / kPage, ceil(L / kPage)).
-__device__ __forceinline__ int row_pages(const SeqRows& r, int b) {
-  const int L = row_len(r, b);
-  return (L + kPage - 1) / kPage - row_lo(r, L) / kPage;
-}
-
 // A unit row u covers rows u*pack .. u*pack+pack-1 (those < n_rows).  With
 // pack > 1 the rows are chunk positions, whose lengths grow by one per
 // position, so the unit reads from the first row's window start to the last

@@ -52,14 +52,6 @@ __device__ __forceinline__ uint32_t e2m1x8_from_f32(const float (&y)[8]) {
   return r;
 }
 
-// One byte of two E2M1 codes -> f16x2 (low nibble in the low half).  Exact.
-__device__ __forceinline__ uint32_t f16x2_from_e2m1x2(uint32_t byte_in_low_bits) {
-  uint32_t r;
-  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n}\n"
-      : "=r"(r) : "r"(byte_in_low_bits));
-  return r;
-}
-
 // Four bytes of a word, each two E2M1 codes -> four f16x2 registers.
 __device__ __forceinline__ void f16x2x4_from_e2m1_word(uint32_t w, uint32_t (&o)[4]) {
   asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
@@ -210,15 +202,6 @@ __device__ __forceinline__ void fence_barrier_init() {
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// Global -> shared bulk copy of `bytes` (multiple of 16, both addresses
-// 16-byte aligned), completing on mbarrier `bar` with a tx-count of `bytes`.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                         uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-      :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
 
 // Tiled TMA load of a 3-D box (coordinates x innermost) into shared memory,
