@@ -385,7 +385,8 @@ struct Stage1Layout {
   static constexpr int kMetaOff = (kRowInfoOff + kRowInfoBytes + 15) / 16 * 16;
   static constexpr int kBarOff = kMetaOff + NWARPS * kMetaWarpBytes;
   static constexpr int kBarBytes = NWARPS * NSTAGE * 8;
-  // unit id, abort flag, TMEM base, redo flag, first unit taken
+  // unit id, abort flag, TMEM base, redo flag, (unused), next unit, its
+  // work-list word
   static constexpr int kMiscOff = kBarOff + kBarBytes;
   static constexpr int kQOff = (kMiscOff + 32 + 127) / 128 * 128;
   static constexpr int kQRowBytes = kHeadDim * 2 + 16;       // padded: conflict-free ldmatrix
@@ -419,7 +420,6 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
     for (int i = 0; i < NWARPS * NSTAGE; ++i) mbar_init(smem_base + Lay::kBarOff + 8 * i, 1);
     s_misc[1] = 0;
     s_misc[3] = 0;
-    s_misc[4] = 0;
     fence_barrier_init();
   }
   if constexpr (Lay::kTmemO) {
@@ -442,19 +442,21 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
   uint32_t stage_ok = 0;     // bit s: stage s holds a page that was really copied
   const int ta = 2 * c, tb = 2 * c + 1, tcc = 2 * c + 8, td = 2 * c + 9;
 
+  // The next unit and its work-list word (s_misc[5], s_misc[6]): a CTA's
+  // first unit is its own index (the plan starts the counter at the grid
+  // size); later ones are taken from the counter during the previous unit's
+  // merge, so that the next unit's copies go out without waiting on it.
+  if (threadIdx.x == 0) {
+    s_misc[5] = (int)blockIdx.x;
+    s_misc[6] = (int)blockIdx.x < n_units ? (int)ws.units[blockIdx.x] : 0;
+  }
+
   for (;;) {
-    // A CTA's first unit is its own index (the plan starts the counter at
-    // the grid size); later ones come from the counter.  A CTA that gave up
-    // (its abort flag is set before the merge barriers) takes no more, so
-    // that no unit is taken and then left undone.
-    if (threadIdx.x == 0) {
-      s_misc[0] = s_misc[1] ? n_units : (s_misc[4] ? atomicAdd(&ws.hdr[1], 1) : (int)blockIdx.x);
-      s_misc[4] = 1;
-    }
+    if (threadIdx.x == 0) s_misc[0] = s_misc[1] ? n_units : s_misc[5];
     __syncthreads();
     const int u = s_misc[0];
     if (u >= n_units || s_misc[1]) break;
-    const uint32_t unit = ws.units[u];
+    const uint32_t unit = (uint32_t)s_misc[6];
     const int b = (int)(unit & 0xffffu), split = (int)((unit >> 16) & 0xffu), g = (int)(unit >> 24);
     const int L = GEN ? unit_len(rows, b) : row_len(rows, b);
     const int pps = ws.seq_info[b].x;
@@ -915,6 +917,11 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
           st[2] = l_run[nt][h];
         }
     }
+    // The next unit is taken now; its word is read during the merge below.
+    // A CTA that gave up (its abort flag is set before the merge barriers)
+    // takes no more, so that no unit is taken and then left undone.
+    int next_u = n_units;
+    if (threadIdx.x == 0 && !s_misc[1]) next_u = atomicAdd(&ws.hdr[1], 1);
     __syncthreads();
     const int out_rows = QG * pack;   // rows 0 .. out_rows-1 may be written
     // output row (sequence or chunk position, query head) of unit row r
@@ -942,6 +949,9 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
       ri[NWARPS] = Ls > 0.f ? M + fast_log2(Ls) : -INFINITY;
       ws.part_lse[orow * S + split] = ri[NWARPS];
     }
+    // the next unit's work-list word, in flight while the parts are merged
+    int next_word = 0;
+    if (threadIdx.x == 0 && next_u < n_units) next_word = (int)ws.units[next_u];
     // Lane (gq, c) holds head dims 32gq .. 32gq+31 of rows nt*8 + 2c (+1);
     // the head dims are merged in kMergeParts parts through one buffer.
 #pragma unroll
@@ -1000,9 +1010,13 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
       }
       __syncthreads();  // the merge buffer (the stage buffers) and Q' are free again
     }
-    if (threadIdx.x == 0 && s_misc[3]) {
-      ws.redo[atomicAdd(&ws.hdr[2], 1)] = (uint32_t)u;
-      s_misc[3] = 0;
+    if (threadIdx.x == 0) {
+      if (s_misc[3]) {
+        ws.redo[atomicAdd(&ws.hdr[2], 1)] = (uint32_t)u;
+        s_misc[3] = 0;
+      }
+      s_misc[5] = next_u;
+      s_misc[6] = next_word;
     }
   }
   if constexpr (Lay::kTmemO) {
