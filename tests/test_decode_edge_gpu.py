@@ -170,6 +170,53 @@ def test_k_block_spread_on_some_tokens(Hq, Hk, every):
     compare(out, _oracle(wl, ref_cache, q_bits))
 
 
+@pytest.mark.parametrize("Hq,Hk", GROUPS)
+def test_k_block_spread_under_graph_replay(Hq, Hk):
+    """One captured decode replayed with new lengths over a cache whose far
+    K blocks (2^40, query rows zero there) sit only from token 400 on: the
+    exact pass's list is rebuilt on every replay, from empty (all lengths
+    below 400) to every unit of the long sequences, and each replay matches
+    both the oracle and an eager call."""
+    rng = np.random.default_rng(1250 + Hq)
+    lens = [3, 700, 1500, 64]
+    wl = _layout(lens, Hq, Hk, seed=15, splits=6)
+    n = int(np.sum(lens))
+    kr = _rows(rng, n, Hk)
+    starts = np.concatenate([[0], np.cumsum(lens)[:-1]])
+    for b, L in enumerate(lens):
+        kr[starts[b] + 400:starts[b] + L, :, 224:256] *= np.float32(2.0 ** 40)
+    vv = _rows(rng, n, Hk)
+    ref_cache = _fill(wl, kr, vv)
+    qp = rng.integers(-2, 3, size=(wl.B, Hq, D)).astype(np.float64)
+    qp[..., 224:256] = 0.0
+    q_bits = _query_from_prime(qp)
+    dev = "cuda"
+    cache = torch.from_numpy(ref_cache).to(dev)
+    q = torch.from_numpy(q_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    bt = torch.from_numpy(wl.block_table).to(dev)
+    sl = torch.from_numpy(wl.seq_lens).to(dev)
+    ws = torch.empty(binding.uq_decode_workspace_bytes(wl.B, wl.Hq, D, wl.splits), dtype=torch.uint8, device=dev)
+    out = torch.empty((wl.B, wl.Hq, D), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        binding.uq_decode(q, cache, bt, sl, wl.scale, wl.splits, ws, out)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        binding.uq_decode(q, cache, bt, sl, wl.scale, wl.splits, ws, out)
+    for new_lens in ([3, 700, 1500, 64], [3, 399, 390, 64], [0, 401, 1500, 0], [3, 700, 1500, 64]):
+        nl = np.array(new_lens, np.int32)
+        sl.copy_(torch.from_numpy(nl))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert binding.uq_check_device_error() == 0
+        ref = oracle.decode(q_bits, ref_cache, wl.block_table, nl, wl.scale)
+        compare(out, ref)
+        eager = torch.empty_like(out)
+        binding.uq_decode(q, cache, bt, torch.from_numpy(nl).to(dev), wl.scale, wl.splits, ws, eager)
+        assert torch.equal(out, eager)
+
+
 @pytest.mark.parametrize("Hq,Hk,cached,q_len,block_size", [
     (8, 1, 300, 5, 16),
     (12, 2, 95, 3, 64),
