@@ -699,36 +699,78 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
         // the reduction would have decided too.
         float sv[NT][2][2], uv[NT][2][2];   // [tile][row half][token gq, gq + 8]
         bool grow = false;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          float sres[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            float acc = sacc[nt][0][k];
-#pragma unroll
-            for (int ch = 1; ch < NCH; ++ch) acc += sacc[nt][ch][k];
-            sres[k] = acc;
-          }
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            sv[nt][h][0] = (GEN ? v0r[nt][h] : v0) ? sres[h] * fk0 : -INFINITY;
-            sv[nt][h][1] = (GEN ? v1r[nt][h] : v1) ? sres[2 + h] * fk1 : -INFINITY;
-          }
-        }
         // With rows of different lengths in one unit (GEN), a row can meet a
         // page with none of its tokens before any page with one; its maximum
         // is still -inf, and 0 stands in so that exp2 gives 0.
+        //
+        // The 16-row kernel runs the fp32 steps here and below on packed
+        // pairs (the two row halves h of a token; two values per
+        // instruction, each rounded as on its own, so the results are those
+        // of the scalar form).  The 8-row kernel measured faster scalar.
+        constexpr bool kPacked = NT == 2;
+        const float2 neg1 = make_float2(-1.f, -1.f);
+        if constexpr (kPacked) {
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+          for (int nt = 0; nt < NT; ++nt) {
+            float2 a01 = make_float2(sacc[nt][0][0], sacc[nt][0][1]);   // token gq, rows 2c, 2c+1
+            float2 a23 = make_float2(sacc[nt][0][2], sacc[nt][0][3]);   // token gq + 8
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const float s0 = sv[nt][h][0], s1 = sv[nt][h][1];
-            const float m_ref = GEN && m_run[nt][h] == -INFINITY ? 0.f : m_run[nt][h];
-            uv[nt][h][0] = (s0 - m_ref) + evf0;
-            uv[nt][h][1] = (s1 - m_ref) + evf1;
-            grow |= fmaxf(s0, s1) > m_run[nt][h] + kLazyMaxLog2;
-            grow |= fmaxf(uv[nt][h][0], uv[nt][h][1]) > d_run[nt][h] + kLazyMaxLog2;
+            for (int ch = 1; ch < NCH; ++ch) {
+              a01 = __fadd2_rn(a01, make_float2(sacc[nt][ch][0], sacc[nt][ch][1]));
+              a23 = __fadd2_rn(a23, make_float2(sacc[nt][ch][2], sacc[nt][ch][3]));
+            }
+            const float2 s01 = __fmul2_rn(a01, make_float2(fk0, fk0));
+            const float2 s23 = __fmul2_rn(a23, make_float2(fk1, fk1));
+            sv[nt][0][0] = (GEN ? v0r[nt][0] : v0) ? s01.x : -INFINITY;
+            sv[nt][1][0] = (GEN ? v0r[nt][1] : v0) ? s01.y : -INFINITY;
+            sv[nt][0][1] = (GEN ? v1r[nt][0] : v1) ? s23.x : -INFINITY;
+            sv[nt][1][1] = (GEN ? v1r[nt][1] : v1) ? s23.y : -INFINITY;
+            const float2 m2 = make_float2(GEN && m_run[nt][0] == -INFINITY ? 0.f : m_run[nt][0],
+                                          GEN && m_run[nt][1] == -INFINITY ? 0.f : m_run[nt][1]);
+            // (s - m_ref) + e_V, s - m_ref as fma(m_ref, -1, s)
+            const float2 u0 = __fadd2_rn(__ffma2_rn(m2, neg1, make_float2(sv[nt][0][0], sv[nt][1][0])),
+                                         make_float2(evf0, evf0));
+            const float2 u1 = __fadd2_rn(__ffma2_rn(m2, neg1, make_float2(sv[nt][0][1], sv[nt][1][1])),
+                                         make_float2(evf1, evf1));
+            uv[nt][0][0] = u0.x;
+            uv[nt][1][0] = u0.y;
+            uv[nt][0][1] = u1.x;
+            uv[nt][1][1] = u1.y;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              grow |= fmaxf(sv[nt][h][0], sv[nt][h][1]) > m_run[nt][h] + kLazyMaxLog2;
+              grow |= fmaxf(uv[nt][h][0], uv[nt][h][1]) > d_run[nt][h] + kLazyMaxLog2;
+            }
           }
+        } else {
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            float sres[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              float acc = sacc[nt][0][k];
+#pragma unroll
+              for (int ch = 1; ch < NCH; ++ch) acc += sacc[nt][ch][k];
+              sres[k] = acc;
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              sv[nt][h][0] = (GEN ? v0r[nt][h] : v0) ? sres[h] * fk0 : -INFINITY;
+              sv[nt][h][1] = (GEN ? v1r[nt][h] : v1) ? sres[2 + h] * fk1 : -INFINITY;
+            }
+          }
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const float s0 = sv[nt][h][0], s1 = sv[nt][h][1];
+              const float m_ref = GEN && m_run[nt][h] == -INFINITY ? 0.f : m_run[nt][h];
+              uv[nt][h][0] = (s0 - m_ref) + evf0;
+              uv[nt][h][1] = (s1 - m_ref) + evf1;
+              grow |= fmaxf(s0, s1) > m_run[nt][h] + kLazyMaxLog2;
+              grow |= fmaxf(uv[nt][h][0], uv[nt][h][1]) > d_run[nt][h] + kLazyMaxLog2;
+            }
+        }
         bool rescale = false;
         float alpha[NT][2];   // O's factor where the V reference moved
         if (__any_sync(0xffffffffu, grow)) {
@@ -758,19 +800,40 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
             }
         }
         uint32_t pw[NT][2];
+        if constexpr (kPacked) {
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          float w4[4];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const float m_ref = GEN && m_run[nt][h] == -INFINITY ? 0.f : m_run[nt][h];
-            const float d_ref = GEN && d_run[nt][h] == -INFINITY ? 0.f : d_run[nt][h];
-            l_run[nt][h] += fast_exp2(sv[nt][h][0] - m_ref) + fast_exp2(sv[nt][h][1] - m_ref);
-            w4[h] = fast_exp2(uv[nt][h][0] - d_ref);
-            w4[2 + h] = fast_exp2(uv[nt][h][1] - d_ref);
+          for (int nt = 0; nt < NT; ++nt) {
+            const float2 m2 = make_float2(GEN && m_run[nt][0] == -INFINITY ? 0.f : m_run[nt][0],
+                                          GEN && m_run[nt][1] == -INFINITY ? 0.f : m_run[nt][1]);
+            const float2 d2 = make_float2(GEN && d_run[nt][0] == -INFINITY ? 0.f : d_run[nt][0],
+                                          GEN && d_run[nt][1] == -INFINITY ? 0.f : d_run[nt][1]);
+            const float2 e0 = __ffma2_rn(m2, neg1, make_float2(sv[nt][0][0], sv[nt][1][0]));
+            const float2 e1 = __ffma2_rn(m2, neg1, make_float2(sv[nt][0][1], sv[nt][1][1]));
+            const float2 x0 = make_float2(fast_exp2(e0.x), fast_exp2(e0.y));
+            const float2 x1 = make_float2(fast_exp2(e1.x), fast_exp2(e1.y));
+            const float2 l2 = __fadd2_rn(make_float2(l_run[nt][0], l_run[nt][1]), __fadd2_rn(x0, x1));
+            l_run[nt][0] = l2.x;
+            l_run[nt][1] = l2.y;
+            const float2 f0 = __ffma2_rn(d2, neg1, make_float2(uv[nt][0][0], uv[nt][1][0]));
+            const float2 f1 = __ffma2_rn(d2, neg1, make_float2(uv[nt][0][1], uv[nt][1][1]));
+            pw[nt][0] = movmatrix_trans(pack_f16x2(fast_exp2(f0.x), fast_exp2(f0.y)));
+            pw[nt][1] = movmatrix_trans(pack_f16x2(fast_exp2(f1.x), fast_exp2(f1.y)));
           }
-          pw[nt][0] = movmatrix_trans(pack_f16x2(w4[0], w4[1]));
-          pw[nt][1] = movmatrix_trans(pack_f16x2(w4[2], w4[3]));
+        } else {
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            float w4[4];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const float m_ref = GEN && m_run[nt][h] == -INFINITY ? 0.f : m_run[nt][h];
+              const float d_ref = GEN && d_run[nt][h] == -INFINITY ? 0.f : d_run[nt][h];
+              l_run[nt][h] += fast_exp2(sv[nt][h][0] - m_ref) + fast_exp2(sv[nt][h][1] - m_ref);
+              w4[h] = fast_exp2(uv[nt][h][0] - d_ref);
+              w4[2 + h] = fast_exp2(uv[nt][h][1] - d_ref);
+            }
+            pw[nt][0] = movmatrix_trans(pack_f16x2(w4[0], w4[1]));
+            pw[nt][1] = movmatrix_trans(pack_f16x2(w4[2], w4[3]));
+          }
         }
         if (__any_sync(0xffffffffu, rescale)) {
           if constexpr (Lay::kTmemO) {
