@@ -102,7 +102,10 @@ size_t uq_decode_workspace_bytes(int B, int Hq, int head_dim, int max_num_kv_spl
  *   slot_mapping  int64 [num_tokens]; token n goes to slot slot_mapping[n]
  *                 (page = slot / block_size, offset = slot % block_size).
  *                 A negative slot skips the token; a slot >= num_blocks *
- *                 block_size skips it and sets UQ_DEVERR_BAD_SLOT.
+ *                 block_size skips it and sets UQ_DEVERR_BAD_SLOT.  A
+ *                 skipped token's K and V rows are still read (they must
+ *                 be valid memory like every other row); only its slot is
+ *                 not written.
  *
  * Per (token, head): K is converted to fp32 (exact), transformed by the
  * unnormalised fast Walsh-Hadamard butterfly in the fixed stage order

@@ -50,6 +50,28 @@ def test_store_ragged_row_counts(N, Hk):
     assert np.array_equal(cache.cpu().numpy(), _oracle_store(k, v, slots, shape))
 
 
+@pytest.mark.parametrize("N,Hk", [(9000, 5), (5000, 7)])
+def test_store_several_passes_of_the_persistent_grid(N, Hk):
+    """More (token, kv head) rows than the resident CTAs take in one pass
+    (3 per SM x 32 rows), with Hk not dividing the pass, so each group's
+    token and head advance with a carry; some slots negative, one out of
+    range."""
+    g = torch.Generator(device="cuda").manual_seed(200 + Hk)
+    k = torch.randn((N, Hk, 256), generator=g, device="cuda").to(torch.bfloat16)
+    v = (torch.randn((N, Hk, 256), generator=g, device="cuda") * 2).to(torch.bfloat16)
+    nb = (N + 15) // 16 + 3
+    slots = torch.randperm(nb * 16, generator=g, device="cuda")[:N].to(torch.int64)
+    slots[::97] = -1
+    slots[N // 2] = nb * 16 + 5
+    shape = (nb, 16, Hk, 272)
+    cache = torch.zeros(shape, dtype=torch.uint8, device="cuda")
+    binding.uq_store(k, v, cache, slots)
+    assert binding.uq_check_device_error() & binding.UQ_DEVERR_BAD_SLOT
+    ok = slots.clone()
+    ok[N // 2] = -1
+    assert np.array_equal(cache.cpu().numpy(), _oracle_store(k, v, ok, shape))
+
+
 def test_store_strided_rows_and_skipped_slots():
     N, Hk = 40, 3
     g = torch.Generator(device="cuda").manual_seed(7)
