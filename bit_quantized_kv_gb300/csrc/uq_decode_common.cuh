@@ -56,7 +56,7 @@ constexpr uint32_t kTmemCols = 128;
 constexpr int kTmemCtasPerSm = UQ_S1_NT2_MIN_BLOCKS;
 // The general 16-row instantiation (windows, larger pages, multi-query units)
 // runs 4 CTAs per SM at 128 registers: measured 9.7% faster on a multi-query
-// chunk, where the plain copy at 4 CTAs is 2.5% slower on a long batch.
+// chunk, where the plain copy at 4 CTAs is 3.5% slower on a long batch.
 #ifndef UQ_S1_NT2_GEN_MIN_BLOCKS
 #define UQ_S1_NT2_GEN_MIN_BLOCKS 4
 #endif
