@@ -736,11 +736,13 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
             uv[nt][1][0] = u0.y;
             uv[nt][0][1] = u1.x;
             uv[nt][1][1] = u1.y;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              grow |= fmaxf(sv[nt][h][0], sv[nt][h][1]) > m_run[nt][h] + kLazyMaxLog2;
-              grow |= fmaxf(uv[nt][h][0], uv[nt][h][1]) > d_run[nt][h] + kLazyMaxLog2;
-            }
+            const float2 lazy = make_float2(kLazyMaxLog2, kLazyMaxLog2);
+            const float2 mt = __fadd2_rn(make_float2(m_run[nt][0], m_run[nt][1]), lazy);
+            const float2 dt = __fadd2_rn(make_float2(d_run[nt][0], d_run[nt][1]), lazy);
+            grow |= fmaxf(sv[nt][0][0], sv[nt][0][1]) > mt.x;
+            grow |= fmaxf(sv[nt][1][0], sv[nt][1][1]) > mt.y;
+            grow |= fmaxf(uv[nt][0][0], uv[nt][0][1]) > dt.x;
+            grow |= fmaxf(uv[nt][1][0], uv[nt][1][1]) > dt.y;
           }
         } else {
 #pragma unroll
