@@ -1183,8 +1183,23 @@ decode_stage2(Workspace ws, int B, int Hq, int S, int pack, const float* __restr
   const int b = row / Hq;
   const int n = ws.seq_info[b / pack].y;   // row b's unit row holds its split count
   const float* lse = ws.part_lse + (int64_t)row * S;
-  float mx = -INFINITY;
-  for (int s = lane; s < n; s += 32) mx = fmaxf(mx, lse[s]);
+  const float* po = ws.part_o + (int64_t)row * S * kHeadDim + lane * 8;
+  // The first 32 splits' log-sum-exps are loaded before the split count
+  // arrives (slots past it hold stale words and are never used), and the
+  // first kSpec splits' partials all at once as soon as it has, so a row's
+  // reads take two round trips instead of a chain.
+  constexpr int kSpec = 8;
+  const float lse_lane = lane < S ? lse[lane] : -INFINITY;
+  float4 vs[kSpec][2];
+#pragma unroll
+  for (int i = 0; i < kSpec; ++i) {
+    if (i < n) {
+      vs[i][0] = *reinterpret_cast<const float4*>(po + (int64_t)i * kHeadDim);
+      vs[i][1] = *reinterpret_cast<const float4*>(po + (int64_t)i * kHeadDim + 4);
+    }
+  }
+  float mx = lane < n ? lse_lane : -INFINITY;
+  for (int s = lane + 32; s < n; s += 32) mx = fmaxf(mx, lse[s]);
 #pragma unroll
   for (int msk = 16; msk > 0; msk >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, msk));
   // a sink logit joins the denominator only (log2 units like the partials)
@@ -1194,26 +1209,33 @@ decode_stage2(Workspace ws, int B, int Hq, int S, int pack, const float* __restr
   // weighted by its share (<= 1): the running sum never exceeds the largest
   // split output in magnitude, even next to fp32's top
   float den = 0.f;
-  if (mx > -INFINITY)
-    for (int s = lane; s < n; s += 32) den += fast_exp2(lse[s] - mx);
+  if (mx > -INFINITY) {
+    if (lane < n) den += fast_exp2(lse_lane - mx);
+    for (int s = lane + 32; s < n; s += 32) den += fast_exp2(lse[s] - mx);
+  }
 #pragma unroll
   for (int msk = 16; msk > 0; msk >>= 1) den += __shfl_xor_sync(0xffffffffu, den, msk);
   if (zs > -INFINITY) den += fast_exp2(zs - mx);
   const float inv = den > 0.f ? 1.f / den : 0.f;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   if (n > 0 && mx > -INFINITY) {
-    const float* po = ws.part_o + (int64_t)row * S * kHeadDim + lane * 8;
     for (int s0 = 0; s0 < n; s0 += 32) {
-      const float wl = (s0 + lane < n) ? fast_exp2(lse[s0 + lane] - mx) * inv : 0.f;
+      const float wl = (s0 + lane < n) ? fast_exp2((s0 == 0 ? lse_lane : lse[s0 + lane]) - mx) * inv : 0.f;
       const int cnt = min(32, n - s0);
       auto add = [&](int k, const float4& v0, const float4& v1) {
         const float w = __shfl_sync(0xffffffffu, wl, k);
         acc[0] += w * v0.x; acc[1] += w * v0.y; acc[2] += w * v0.z; acc[3] += w * v0.w;
         acc[4] += w * v1.x; acc[5] += w * v1.y; acc[6] += w * v1.z; acc[7] += w * v1.w;
       };
-      // four splits' partials are loaded before any is used, so their
-      // latencies overlap; the sums keep the split order
       int k = 0;
+      if (s0 == 0) {
+#pragma unroll
+        for (int i = 0; i < kSpec; ++i)
+          if (i < cnt) add(i, vs[i][0], vs[i][1]);
+        k = kSpec;
+      }
+      // later splits: four partials are loaded before any is used, so
+      // their latencies overlap; the sums keep the split order
       for (; k + 4 <= cnt; k += 4) {
         float4 v[4][2];
 #pragma unroll
