@@ -38,13 +38,16 @@
 //   QK:  S[t, r] = sum_d K'[t, d] Q'[r, d]      (M = 16 tokens, N = 8 rows)
 //   PV:  O^T[d, r] += sum_t V'[t, d] W[r, t]    (M = 16 head dims, N = 8 rows)
 // Every FP4 value is c * 2^(e_blk - 127).  For each token t the largest
-// block exponent E_t is factored out, so K' = c * 2^(e_blk - E_t) and
-// V' = c * 2^(e_blk - E_t) are exact in f16 whenever e_blk >= E_t - 14; a
-// block more than 2^14 below the token's largest block is dropped (its
-// share of a score or an output is below 2^-14, and every kept factor is a
-// normal f16).  2^(E^K_t - 127) multiplies the scores;
-// 2^(E^V_t - 127) is added to the exponent of the probability that weights
-// the token's V' row.  The contraction index of QK may be permuted freely as
+// block exponent E_t is factored out: K' = c * 2^(13 + e_blk - E_t) and
+// V' = c * 2^(13 + e_blk - E_t) are exact f16 values for e_blk > E_t - 28
+// (every kept factor is a normal f16, the largest code 6 * 2^13 stays inside
+// f16's range).  2^(E^K_t - 127 - 13) multiplies the scores;
+// E^V_t - 127 - 13 is added to the exponent of the probability that weights
+// the token's V' row.  A K block 2^28 or more below its token's largest
+// block turns that token's score factor NaN, and the unit is redone in
+// plain fp32 by the exact pass; a V block that far below its token's
+// largest block is dropped (its share of an output is below 2^-28 of that
+// token's).  The contraction index of QK may be permuted freely as
 // long as Q' and K' agree, which lets every lane read contiguous bytes:
 // lane (g = lane/4, c = lane%4) owns head dims [64c, 64c+64) of K (k-step i
 // covers 64c + 4i .. +3) and V head dims [32g, 32g+32) (one UE8M0 block).
