@@ -397,9 +397,11 @@ struct Stage1Layout {
   static constexpr int kBytes = kQOff + kQBytes;
 };
 
-// GEN: a sliding window or pages of more than 16 tokens.  The plain
-// instantiation (block_size 16, no window) folds both away.
-template <int NT, int NWARPS, int NSTAGE, bool GEN>
+// GEN: 0 plain (block_size 16, no window, one query row per sequence);
+// 1 multi-query unit rows only (rows of their own lengths; block_size 16,
+// no window), which folds the window start and the page-size shifts away;
+// 2 general (a sliding window or pages of more than 16 tokens as well).
+template <int NT, int NWARPS, int NSTAGE, int GEN>
 __global__ void __launch_bounds__(NWARPS * 32, NT == 1 ? UQ_S1_MIN_BLOCKS : (GEN ? kTmemCtasPerSmGen : kTmemCtasPerSm))
 decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
               const __grid_constant__ CUtensorMap kv_map, const uint8_t* __restrict__ kv,
@@ -464,7 +466,7 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
     const int L = GEN ? unit_len(rows, b) : row_len(rows, b);
     const int pps = ws.seq_info[b].x;
     const int P = (L + kPage - 1) / kPage;
-    const int lo = GEN ? unit_lo(rows, b) : 0;   // first token of the window
+    const int lo = GEN == 2 ? unit_lo(rows, b) : 0;   // first token of the window
     // Query rows of the unit: row r is query head g*QG + r % QG of row
     // b*pack + r / QG (pack > 1 only for multi-query chunk positions).
     const int pack = GEN ? rows.pack : 1;
@@ -480,10 +482,10 @@ decode_stage1(const uint16_t* __restrict__ query, int64_t q_ss, int64_t q_sh,
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           rhi[nt][h] = row_len(rows, row_of(nt * 8 + 2 * c + h));
-          rlo[nt][h] = row_lo(rows, rhi[nt][h]);
+          rlo[nt][h] = GEN == 2 ? row_lo(rows, rhi[nt][h]) : 0;
         }
     }
-    const int lg_tpp = GEN ? rows.lg_tpp : 0;
+    const int lg_tpp = GEN == 2 ? rows.lg_tpp : 0;
     const int p_begin = lo / kPage + split * pps;
     const int p_end = min(p_begin + pps, P);
 
@@ -1305,7 +1307,7 @@ static cudaError_t launch_overlapped(void (*kern)(Params...), dim3 grid, dim3 bl
 cudaError_t current_context_id(unsigned long long* id);
 static std::mutex g_grid_mutex;
 
-template <int NT, bool GEN>
+template <int NT, int GEN>
 static cudaError_t stage1_grid(int* grid) {
   constexpr int NWARPS = 4, NSTAGE = kStage1Stages;
   using Lay = Stage1Layout<NT, NWARPS, NSTAGE>;
@@ -1382,7 +1384,7 @@ cudaError_t make_kv_tensor_map(CUtensorMap* map, const uint8_t* kv, int Hk, int6
 }
 
 // Plan, then stage 1 (bracketed by the caller's timing events, if any).
-template <int NT, bool GEN>
+template <int NT, int GEN>
 static cudaError_t launch_plan_and_stage1(const uint16_t* query, int64_t q_ss, int64_t q_sh,
                                           const uint8_t* kv, const int32_t* bt, const SeqRows& sl,
                                           float scale, int B, int Hq, int Hk, int num_blocks,
@@ -1406,7 +1408,7 @@ static cudaError_t launch_plan_and_stage1(const uint16_t* query, int64_t q_ss, i
                         num_blocks, S, ws, err);
   if (e != cudaSuccess) return e;
   if (ev_after && (e = record_timing_event(ev_after, stream)) != cudaSuccess) return e;
-  return launch_overlapped(decode_exact_units<GEN>, dim3((grid + 3) / 4), dim3(kExactWarps * 32), 0, stream, query,
+  return launch_overlapped(decode_exact_units<(GEN != 0)>, dim3((grid + 3) / 4), dim3(kExactWarps * 32), 0, stream, query,
                            q_ss, q_sh, kv, bt, sl, scale * kLog2e, Hq, Hk, Hq / Hk, num_blocks, S, ws);
 }
 
@@ -1418,7 +1420,8 @@ cudaError_t launch_decode(const uint16_t* query, int64_t q_ss, int64_t q_sh, con
                           void* workspace, uint16_t* out, unsigned* err, cudaStream_t stream,
                           cudaEvent_t ev_before_stage1, cudaEvent_t ev_after_stage1) {
   const Workspace ws = workspace_layout(workspace, B, Hq, S);
-  const bool gen = sl.window > 0 || sl.lg_tpp > 0 || sl.pack > 1;
+  // 2: a window or pages of more than 16 tokens; 1: multi-query unit rows only
+  const int gen = (sl.window > 0 || sl.lg_tpp > 0) ? 2 : (sl.pack > 1 ? 1 : 0);
   const bool sixteen = (Hq / Hk) * sl.pack > 8;
   auto run = [&](auto nt, auto g) {
     return launch_plan_and_stage1<decltype(nt)::value, decltype(g)::value>(
@@ -1427,10 +1430,13 @@ cudaError_t launch_decode(const uint16_t* query, int64_t q_ss, int64_t q_sh, con
   };
   using One = std::integral_constant<int, 1>;
   using Two = std::integral_constant<int, 2>;
-  using Gen = std::true_type;
-  using Plain = std::false_type;
-  cudaError_t e = sixteen ? (gen ? run(Two{}, Gen{}) : run(Two{}, Plain{}))
-                          : (gen ? run(One{}, Gen{}) : run(One{}, Plain{}));
+  using Plain = std::integral_constant<int, 0>;
+  using MqRows = std::integral_constant<int, 1>;
+  using Gen = std::integral_constant<int, 2>;
+  // 8-row units never hold two chunk positions (6- and 8-row groups pack
+  // into 16-row units), so they take the general kernel for any GEN case
+  cudaError_t e = sixteen ? (gen == 2 ? run(Two{}, Gen{}) : gen == 1 ? run(Two{}, MqRows{}) : run(Two{}, Plain{}))
+                          : (gen != 0 ? run(One{}, Gen{}) : run(One{}, Plain{}));
   if (e != cudaSuccess) return e;
   const int rows = B * Hq;
   return launch_overlapped(decode_stage2, dim3((rows + 3) / 4), dim3(128), 0, stream, ws, B, Hq, S, sl.pack,
