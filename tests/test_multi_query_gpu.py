@@ -122,3 +122,34 @@ def test_empty_chunk_is_a_noop():
     q = torch.empty((0, 8, 256), dtype=torch.bfloat16, device="cuda")
     _mq(wl, cache, q, 16, 4)
     assert binding.uq_check_device_error() == 0
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_chunks_match_oracle(seed):
+    """Seeded random chunks: 6, 8 or 16 query heads per kv head, 1 to 3 kv
+    heads, 0 to 2999 cached tokens, 1 to 8 chunk rows, 1 to 32 splits, and
+    sometimes a sliding window.  Covers both multi-query kernels (packed
+    chunk rows without a window, and the general one with it) against the
+    oracle's decode of the synthetic batch."""
+    rng = np.random.default_rng(7000 + seed)
+    QG = int(rng.choice([6, 8, 16]))
+    Hk = int(rng.integers(1, 4))
+    cached = int(rng.integers(0, 3000))
+    q_len = int(rng.integers(1, 9))
+    S = int(rng.integers(1, 33))
+    window = int(rng.choice([0, 0, 50, 700]))
+    L = cached + q_len
+    P = (L + 15) // 16
+    wl = workloads.make_decode_workload("mq", 1, QG * Hk, Hk, np.array([L]), P + 2, S, seed=300 + seed,
+                                        spare_blocks=3)
+    cache = fill_cache_gpu(wl)
+    q = workloads.chunk_query(wl, q_len, "cuda")
+    bt = torch.from_numpy(np.ascontiguousarray(wl.block_table[0])).cuda()
+    ws = torch.empty(binding.uq_decode_workspace_bytes(q_len, wl.Hq, 256, S), dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(q)
+    binding.uq_decode_multi_query(q, cache, bt, cached, wl.scale, S, ws, out, sliding_window=window)
+    assert binding.uq_check_device_error() == 0
+    ref_cache = oracle_cache_for_sequence(wl, 0)
+    table = np.tile(np.arange(P, dtype=np.int32), (q_len, 1))
+    lens = (cached + 1 + np.arange(q_len)).astype(np.int32)
+    compare(out, oracle.decode(bits(q), ref_cache, table, lens, wl.scale, window=window))
